@@ -1,0 +1,259 @@
+"""Float64 CPU oracle for long-context prefill attention (dense and block-sparse).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or run
+anything under ``oracle/``.  The CUDA library never calls it, and it shares no
+code, header, table or helper with the CUDA path: its inputs are plain float64
+numpy arrays (exact upcasts of the fp16/bf16 inputs).
+
+Each function is the plain definition written out, row by row, with a numpy
+matmul as the only library step: no tiling, no online softmax, no fusion.
+Rows are computed in groups only to bound memory; every row's result depends
+on that row alone.
+
+Sources (page title, section):
+  * "Flash attention on ANE: fast long-context prefill", section
+    "Flash attention: the core insight" -- softmax(Q K^T) V computed per query
+    row; tiling is an implementation of the same result, so the oracle uses
+    the untiled form.
+  * "ANE Prefill Research", sections "How the ANE prefill path works" (a chunk
+    of queries attends to a token-major K/V history plus its own keys, under
+    an additive mask; the chunk's K/V are returned in cache layout) and
+    "Folding a sparse indexer's selection into the mask" (dropped keys carry
+    -30000, which exp() turns into an exact zero).
+  * "The Four Principles for Optimizing Transformers on the ANE", section
+    "Masking in this layout" (masks are additive floats applied before the
+    softmax).
+  * "Porting FlashPrefill V2 to Apple silicon for faster prefill", sections
+    "Compress keys before the heavy work" (mean-pool each key block),
+    "A cheap map of where the attention lives" (one pooled score per query
+    row per block; the local block stays exact), "The algorithm starts here"
+    (keep blocks above alpha x the row's hottest block, plus the diagonal) and
+    "Compute the peaks, summarize the rest" (kept blocks exact, skipped blocks
+    represented by their pooled row).  The pooled correction weight is fixed
+    by the benchmark spec: a skipped block b adds n_b * exp(q.kbar_b * scale)
+    to the denominator and that weight times vbar_b to the numerator.
+
+Readings where the pages are silent:
+  * the mask is added after scaling: logits = (q.k) * scale + M;
+  * mask=None means plain causal, the same as a 0 / -30000 causal mask;
+  * with an explicit mask, visibility is the mask alone (it is arbitrary, not
+    causal by contract), over all start_pos + C keys;
+  * GQA: query head h reads KV head floor(h / (Hq / Hkv));
+  * "above alpha x the hottest block" compares probabilities:
+    exp(s_b - s_max) >= alpha; candidates are the strictly earlier blocks
+    b < floor(p / block); the diagonal block floor(p / block) is always kept
+    and never pooled; alpha = 0 keeps every candidate;
+  * selection is per query row and per query head;
+  * n_b is the number of keys in block b (the full block size for every
+    candidate block, since candidates lie strictly before the query's block).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+MASK_DROP = -30000.0
+_ROW_ELEMS = 1 << 24  # rows per group are sized so that a logits group is ~128 MB
+
+
+def _rows_arg(rows, n):
+    return np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+
+
+def _heads_arg(heads, n):
+    return list(range(n)) if heads is None else list(heads)
+
+
+def causal_additive(C: int, start_pos: int, rows=None) -> np.ndarray:
+    """0 where key j <= start_pos + i, else -30000; shape [len(rows), start_pos + C]."""
+    rows = _rows_arg(rows, C)
+    j = np.arange(start_pos + C)[None, :]
+    return np.where(j <= start_pos + rows[:, None], 0.0, MASK_DROP)
+
+
+# --------------------------------------------------------------------------
+# dense chunked prefill
+# --------------------------------------------------------------------------
+def dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, scale=None, rows=None,
+          heads=None):
+    """Attention of a chunk over [history ; chunk] keys.
+
+    q [B, C, Hq, d]; k_hist, v_hist [B, s, Hkv, d]; k_chunk, v_chunk
+    [B, C, Hkv, d]; mask [C, s + C] additive (shared by batch and heads) or
+    None for causal.  For every row i (absolute position p = s + i) and head
+    h: l_j = (q_i . k_j) * scale + M[i, j] over all keys j < s + C,
+    o_i = sum_j exp(l_j - max l) v_j / sum_j exp(l_j - max l).
+    Returns out [B, len(rows), len(heads), d].
+    """
+    B, C, Hq, d = q.shape
+    Hkv = k_chunk.shape[2]
+    G = Hq // Hkv
+    s = int(start_pos)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    k = np.concatenate([k_hist, k_chunk], axis=1)
+    v = np.concatenate([v_hist, v_chunk], axis=1)
+    T = s + C
+    rows = _rows_arg(rows, C)
+    heads = _heads_arg(heads, Hq)
+    out = np.empty((B, len(rows), len(heads), d))
+    step = max(1, _ROW_ELEMS // T)
+    for b in range(B):
+        for hi, h in enumerate(heads):
+            g = h // G
+            kg, vg = k[b, :, g, :], v[b, :, g, :]
+            for r0 in range(0, len(rows), step):
+                rr = rows[r0:r0 + step]
+                logits = (q[b, rr, h, :] @ kg.T) * scale
+                logits += causal_additive(C, s, rr) if mask is None else mask[rr, :]
+                m = logits.max(axis=1, keepdims=True)
+                w = np.exp(logits - m)
+                out[b, r0:r0 + len(rr), hi, :] = (w @ vg) / w.sum(axis=1, keepdims=True)
+    return out
+
+
+def chunk_kv_cache_layout(k_chunk):
+    """The chunk's K (or V) in the head-major cache layout [B, Hkv, C, d]: a pure re-layout."""
+    return np.ascontiguousarray(np.transpose(k_chunk, (0, 2, 1, 3)))
+
+
+# --------------------------------------------------------------------------
+# block-sparse prefill: pooled index
+# --------------------------------------------------------------------------
+def pool_blocks(x, block: int) -> np.ndarray:
+    """Mean of each key block: x [B, T, H, d] -> [B, H, ceil(T / block), d]."""
+    B, T, H, d = x.shape
+    nblk = (T + block - 1) // block
+    out = np.empty((B, H, nblk, d))
+    for bk in range(nblk):
+        out[:, :, bk, :] = x[:, bk * block:min(T, (bk + 1) * block)].mean(axis=1)
+    return out
+
+
+def block_counts(T: int, block: int) -> np.ndarray:
+    nblk = (T + block - 1) // block
+    return np.array([min(T, (bk + 1) * block) - bk * block for bk in range(nblk)], dtype=np.float64)
+
+
+@dataclasses.dataclass
+class Selection:
+    kbar: np.ndarray      # [B, Hkv, nblk, d] pooled keys
+    kept: np.ndarray      # bool [B, R, Hsel, nblk]: row keeps block (diagonal included)
+    near: np.ndarray      # bool [B, R, Hsel]: row has a candidate within 1e-4 relative of alpha
+    scores: np.ndarray    # [B, R, Hsel, nblk] pooled logits (q . kbar) * scale, all blocks
+    rows: np.ndarray
+    heads: list
+    start_pos: int
+    block: int
+
+
+def block_select(q, k, start_pos, block, alpha, scale=None, rows=None, heads=None,
+                 near_rel=1e-4) -> Selection:
+    """Per-row block selection.
+
+    q [B, N, Hq, d] (the chunk's queries), k [B, s + N, Hkv, d] (all keys).
+    For row i at p = s + i: ob = floor(p / block); candidates b < ob;
+    s_ib = (q_i . kbar_b) * scale; keep candidate b iff
+    exp(s_ib - max_c s_ic) >= alpha; the diagonal block ob is always kept.
+    """
+    B, N, Hq, d = q.shape
+    T, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    s = int(start_pos)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kbar = pool_blocks(k, block)
+    nblk = kbar.shape[2]
+    rows = _rows_arg(rows, N)
+    heads = _heads_arg(heads, Hq)
+    ob = (s + rows) // block                                   # [R]
+    cand = np.arange(nblk)[None, :] < ob[:, None]              # [R, nblk]
+    kept = np.zeros((B, len(rows), len(heads), nblk), dtype=bool)
+    near = np.zeros((B, len(rows), len(heads)), dtype=bool)
+    scores = np.empty((B, len(rows), len(heads), nblk))
+    for b in range(B):
+        for hi, h in enumerate(heads):
+            sc = (q[b, rows, h, :] @ kbar[b, h // G].T) * scale   # [R, nblk]
+            scores[b, :, hi] = sc
+            smax = np.where(cand, sc, -np.inf).max(axis=1, keepdims=True)
+            has = cand.any(axis=1)
+            diff = np.where(cand, sc - np.where(has[:, None], smax, 0.0), -np.inf)
+            ratio = np.exp(diff)                                      # p_b / p_max
+            keep = cand & (ratio >= alpha)
+            keep[np.arange(len(rows)), ob] = True
+            kept[b, :, hi] = keep
+            if alpha > 0:
+                near[b, :, hi] = (cand & (np.abs(ratio - alpha) <= near_rel * alpha)).any(axis=1)
+    return Selection(kbar, kept, near, scores, rows, heads, s, block)
+
+
+def tile_union(kept_tile_rows) -> np.ndarray:
+    """Sorted union of the kept blocks of a query tile's rows: kept_tile_rows bool [r, nblk]."""
+    return np.flatnonzero(np.asarray(kept_tile_rows).any(axis=0)).astype(np.int32)
+
+
+# --------------------------------------------------------------------------
+# block-sparse prefill: exact kept blocks + pooled correction
+# --------------------------------------------------------------------------
+def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, sel=None):
+    """Block-sparse attention with pooled correction.
+
+    Row i (p = s + i), head h: kept set K_i from ``block_select``; skipped set
+    R_i = {b < ob} minus K_i; exact keys E_i = {j <= p : floor(j / block) in K_i};
+    with l_j = (q_i . k_j) * scale and s_ib the pooled logits,
+      m = max(max_E l_j, max_R s_ib)
+      o_i = (sum_E e^(l_j - m) v_j + sum_R n_b e^(s_ib - m) vbar_b)
+            / (sum_E e^(l_j - m) + sum_R n_b e^(s_ib - m)).
+    Returns (out [B, R, Hsel, d], sel).
+    """
+    B, N, Hq, d = q.shape
+    T, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    s = int(start_pos)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if sel is None:
+        sel = block_select(q, k, s, block, alpha, scale, rows, heads)
+    rows, heads = sel.rows, sel.heads
+    vbar = pool_blocks(v, block)
+    nb = block_counts(T, block)
+    nblk = len(nb)
+    out = np.empty((B, len(rows), len(heads), d))
+    p_all = s + rows
+    ob_all = p_all // block
+    jblk = np.arange(T) // block
+    step = max(1, _ROW_ELEMS // T)
+    for b in range(B):
+        for hi, h in enumerate(heads):
+            g = h // G
+            kg, vg = k[b, :, g, :], v[b, :, g, :]
+            for r0 in range(0, len(rows), step):
+                sl = slice(r0, r0 + step)
+                rr, p, ob = rows[sl], p_all[sl], ob_all[sl]
+                keep = sel.kept[b, sl, hi]                                   # [r, nblk]
+                exact = keep[:, jblk] & (np.arange(T)[None, :] <= p[:, None])
+                skipped = (np.arange(nblk)[None, :] < ob[:, None]) & ~keep
+                logits = np.where(exact, (q[b, rr, h, :] @ kg.T) * scale, -np.inf)
+                pooled = np.where(skipped, sel.scores[b, sl, hi], -np.inf)
+                m = np.maximum(logits.max(axis=1), pooled.max(axis=1))[:, None]
+                we = np.exp(logits - m)
+                wp = nb[None, :] * np.exp(pooled - m)
+                num = we @ vg + wp @ vbar[b, g]
+                den = we.sum(axis=1) + wp.sum(axis=1)
+                out[b, sl, hi, :] = num / den[:, None]
+    return out, sel
+
+
+def skip_share(sel: Selection) -> float:
+    """Share of off-diagonal candidate (row, block) pairs that were skipped."""
+    ob = (sel.start_pos + sel.rows) // sel.block
+    nblk = sel.kept.shape[-1]
+    cand = np.arange(nblk)[None, :] < ob[:, None]                     # [R, nblk]
+    n_cand = cand.sum() * sel.kept.shape[0] * sel.kept.shape[2]
+    if n_cand == 0:
+        return 0.0
+    kept_cand = (sel.kept & cand[None, :, None, :]).sum()
+    return float(1.0 - kept_cand / n_cand)

@@ -1,0 +1,320 @@
+"""Pins for the float64 oracle, each against something other than the oracle itself.
+
+* brute force: per-element Python loops with math.exp on tiny inputs;
+* closed forms and invariants: V = 1 gives 1; masked keys contribute exactly
+  nothing; shift invariance of a fully masked row; chunked prefill equals
+  one-shot causal prefill; GQA equals MHA over repeated K/V heads;
+* the block-sparse path: alpha = 0 and block-constant keys reduce it to dense
+  causal attention; a hand-worked 36-token toy fixes the selection and a
+  hand-derived row fixes the pooled-correction weight n_b * e^(s_b) and vbar_b;
+* the folded-indexer mask's visible-key budget 512*4 + 3 = 2051.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import prefill_inputs as pi
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def brute_dense_row(qi, keys, vals, mrow, scale):
+    """softmax((q.k) * scale + M) V for one query row, plain loops."""
+    logits = []
+    for j in range(len(keys)):
+        dot = 0.0
+        for a in range(len(qi)):
+            dot += qi[a] * keys[j][a]
+        logits.append(dot * scale + mrow[j])
+    mx = max(logits)
+    w = [math.exp(x - mx) for x in logits]
+    z = math.fsum(w)
+    return [math.fsum(w[j] * vals[j][a] for j in range(len(keys))) / z for a in range(len(vals[0]))]
+
+
+def rand_case(seed, B=2, Hq=4, Hkv=2, C=5, s=3, d=8):
+    g = np.random.default_rng(seed)
+    q = g.standard_normal((B, C, Hq, d))
+    kh, vh = g.standard_normal((B, s, Hkv, d)), g.standard_normal((B, s, Hkv, d))
+    kc, vc = g.standard_normal((B, C, Hkv, d)), g.standard_normal((B, C, Hkv, d))
+    return q, kh, vh, kc, vc
+
+
+@pytest.mark.parametrize("masked", [False, True])
+def test_dense_matches_brute_force(masked):
+    q, kh, vh, kc, vc = rand_case(1)
+    B, C, Hq, d = q.shape
+    s, Hkv = kh.shape[1], kh.shape[2]
+    T = s + C
+    g = np.random.default_rng(2)
+    if masked:
+        mask = g.uniform(-3.0, 0.0, size=(C, T))
+        mask[g.random((C, T)) < 0.3] = -30000.0
+        mask[:, 0] = -1.0  # every row keeps a visible key
+    else:
+        mask = None
+    scale = 0.37
+    out = oracle.dense(q, kh, vh, kc, vc, s, mask=mask, scale=scale)
+    k = np.concatenate([kh, kc], 1)
+    v = np.concatenate([vh, vc], 1)
+    for b in range(B):
+        for h in range(Hq):
+            gg = h // (Hq // Hkv)
+            for i in range(C):
+                if mask is None:
+                    mrow = [0.0 if j <= s + i else -30000.0 for j in range(T)]
+                else:
+                    mrow = list(mask[i])
+                ref = brute_dense_row(list(q[b, i, h]), k[b, :, gg].tolist(), v[b, :, gg].tolist(), mrow, scale)
+                assert np.max(np.abs(out[b, i, h] - ref)) <= 1e-12
+
+
+def test_default_scale_is_inverse_sqrt_d():
+    q, kh, vh, kc, vc = rand_case(3)
+    d = q.shape[-1]
+    a = oracle.dense(q, kh, vh, kc, vc, kh.shape[1])
+    b = oracle.dense(q, kh, vh, kc, vc, kh.shape[1], scale=1.0 / math.sqrt(d))
+    assert np.array_equal(a, b)
+
+
+def test_ones_value_gives_one():
+    q, kh, vh, kc, vc = rand_case(4)
+    out = oracle.dense(q, kh, np.ones_like(vh), kc, np.ones_like(vc), kh.shape[1])
+    assert np.max(np.abs(out - 1.0)) <= 1e-12
+
+
+def test_masked_key_contributes_exactly_zero():
+    q, kh, vh, kc, vc = rand_case(5, C=6, s=4)
+    C, s = q.shape[1], kh.shape[1]
+    g = np.random.default_rng(6)
+    mask = np.where(g.random((C, s + C)) < 0.5, -30000.0, 0.0)
+    mask[:, 1] = 0.0
+    base = oracle.dense(q, kh, vh, kc, vc, s, mask=mask)
+    # perturb V of a key that every row masks; the output must not move a single bit
+    mask[:, 2] = -30000.0
+    base = oracle.dense(q, kh, vh, kc, vc, s, mask=mask)
+    vh2 = vh.copy()
+    vh2[:, 2] += 1e3
+    pert = oracle.dense(q, kh, vh2, kc, vc, s, mask=mask)
+    assert np.array_equal(base, pert)
+
+
+def test_fully_masked_row_is_plain_softmax():
+    """A row whose every key carries -30000 is shift-invariant: it equals the unmasked row."""
+    q, kh, vh, kc, vc = rand_case(7, C=4, s=4)
+    C, s = q.shape[1], kh.shape[1]
+    mask = np.zeros((C, s + C))
+    mask[2, :] = -30000.0
+    a = oracle.dense(q, kh, vh, kc, vc, s, mask=mask)
+    b = oracle.dense(q, kh, vh, kc, vc, s, mask=np.zeros((C, s + C)))
+    assert np.max(np.abs(a[:, 2] - b[:, 2])) <= 1e-9
+    assert np.array_equal(a[:, [0, 1, 3]], b[:, [0, 1, 3]])
+
+
+def test_explicit_causal_mask_equals_default():
+    q, kh, vh, kc, vc = rand_case(8, C=7, s=5)
+    C, s = q.shape[1], kh.shape[1]
+    a = oracle.dense(q, kh, vh, kc, vc, s)
+    b = oracle.dense(q, kh, vh, kc, vc, s, mask=pi.causal_mask(C, s, np.float64))
+    assert np.array_equal(a, b)
+
+
+def test_chunked_equals_one_shot():
+    """Chunks at start 0, 64, 128 over the previous chunks' K/V equal one causal pass over 192 rows."""
+    g = np.random.default_rng(9)
+    B, Hq, Hkv, d, N, C = 1, 4, 2, 16, 192, 64
+    q = g.standard_normal((B, N, Hq, d))
+    k = g.standard_normal((B, N, Hkv, d))
+    v = g.standard_normal((B, N, Hkv, d))
+    one = oracle.dense(q, k[:, :0], v[:, :0], k, v, 0)
+    for s in range(0, N, C):
+        part = oracle.dense(q[:, s:s + C], k[:, :s], v[:, :s], k[:, s:s + C], v[:, s:s + C], s)
+        assert np.max(np.abs(part - one[:, s:s + C])) <= 1e-12
+
+
+def test_gqa_equals_repeated_kv_heads():
+    q, kh, vh, kc, vc = rand_case(10, Hq=6, Hkv=2)
+    s = kh.shape[1]
+    a = oracle.dense(q, kh, vh, kc, vc, s)
+    rep = lambda x: np.repeat(x, 3, axis=2)  # head h of 6 reads KV head h // 3
+    b = oracle.dense(q, rep(kh), rep(vh), rep(kc), rep(vc), s)
+    assert np.max(np.abs(a - b)) <= 1e-15
+
+
+def test_rows_and_heads_subsets_agree():
+    q, kh, vh, kc, vc = rand_case(11, C=9, s=6)
+    s = kh.shape[1]
+    full = oracle.dense(q, kh, vh, kc, vc, s)
+    sub = oracle.dense(q, kh, vh, kc, vc, s, rows=[8, 1, 4], heads=[3, 0])
+    assert np.array_equal(sub, full[:, [8, 1, 4]][:, :, [3, 0]])
+
+
+def test_cache_layout_is_a_relayout():
+    _, _, _, kc, _ = rand_case(12)
+    lay = oracle.chunk_kv_cache_layout(kc)
+    B, C, H, d = kc.shape
+    for b in range(B):
+        for h in range(H):
+            for t in range(C):
+                assert np.array_equal(lay[b, h, t], kc[b, t, h])
+
+
+# --------------------------------------------------------------------------
+# folded indexer mask (the generator's budget)
+# --------------------------------------------------------------------------
+def test_folded_mask_visible_budget():
+    """ANE Prefill Research, 'Folding a sparse indexer's selection': keptBlocks*ratio + (ratio-1) = 2051."""
+    s, C = 2048, 64
+    mask, kept = pi.indexer_fold_mask(77, C, s)
+    counts = (mask == 0.0).sum(axis=1)
+    p = s + np.arange(C)
+    assert np.array_equal(counts, 512 * 4 + (p + 1) % 4)
+    assert counts.max() == 512 * 4 + (4 - 1) == 2051
+    for i in range(C):
+        assert kept[i][-1] == (s + i + 1) // 4 - 1          # newest complete block always kept
+        assert len(set(kept[i].tolist())) == 512
+        assert np.all(mask[i, s + i + 1:] == -30000.0)      # no future key is visible
+
+
+# --------------------------------------------------------------------------
+# block-sparse path
+# --------------------------------------------------------------------------
+def toy36(e_scale=1.0):
+    cfg = json.load(open(os.path.join(GOLDEN, "toy36.json")))["construction"]
+    N, blk, d = cfg["N"], cfg["block"], cfg["d"]
+    t = cfg["t"]
+    q = np.zeros((1, N, 1, d))
+    q[0, :, 0, :] = cfg["q_row"]
+    k = np.zeros((1, N, 1, d))
+    v = np.zeros((1, N, 1, d))
+    for j in range(N):
+        e = (0.5 if j % 2 == 0 else -0.5) * e_scale
+        k[0, j, 0, 0] = t[j // blk] + e
+        v[0, j, 0] = (1.0, e, j // blk, 0.0)
+    return q, k, v, blk, cfg["scale"]
+
+
+@pytest.mark.parametrize("alpha", ["0.2", "0.1", "0.0"])
+def test_toy36_selection(alpha):
+    gold = json.load(open(os.path.join(GOLDEN, "toy36.json")))
+    q, k, v, blk, scale = toy36()
+    sel = oracle.block_select(q, k, 0, blk, float(alpha), scale=scale)
+    assert np.allclose(sel.kbar[0, 0, :, 0], gold["construction"]["t"])
+    for qb, expect in enumerate(gold["kept_by_query_block"][alpha]):
+        for r in range(qb * blk, (qb + 1) * blk):
+            assert np.flatnonzero(sel.kept[0, r, 0]).tolist() == expect
+        assert oracle.tile_union(sel.kept[0, qb * blk:(qb + 1) * blk, 0]).tolist() == expect
+    assert not sel.near.any()
+    n_off = sum(len(e) - 1 for e in gold["kept_by_query_block"][alpha]) * blk
+    assert n_off == gold["kept_offdiag_pairs"][alpha]
+    assert abs(oracle.skip_share(sel) - (1 - n_off / gold["candidate_pairs"])) < 1e-12
+
+
+def test_toy36_pooled_correction_closed_form():
+    """Row 12 of the toy at alpha 0.2, derived by hand.
+
+    Kept {1, 2}, skipped {0}.  Exact logits: block 1 keys 3 +- 0.5 (three each),
+    key 12 (block 2) 1 + 0.5; block 0 is represented by one pooled logit t_0 = 0
+    with weight n_0 = 6 and value vbar_0 = (1, 0, 0, 0).
+    """
+    q, k, v, blk, scale = toy36()
+    out, _ = oracle.sparse(q, k, v, 0, blk, 0.2, scale=scale, rows=[12])
+    e35, e25, e15 = math.exp(3.5), math.exp(2.5), math.exp(1.5)
+    den = 3 * e35 + 3 * e25 + e15 + 6 * math.exp(0.0)
+    expect = [1.0,
+              (3 * e35 * 0.5 - 3 * e25 * 0.5 + e15 * 0.5 + 6 * 0.0) / den,
+              ((3 * e35 + 3 * e25) * 1 + e15 * 2 + 6 * 0.0) / den,
+              0.0]
+    assert np.max(np.abs(out[0, 0, 0] - expect)) <= 1e-14
+    # the dense row differs (block 0 exact: logits +-0.5) -- the correction is live
+    dense = oracle.dense(q, k[:, :0], v[:, :0], k, v, 0, scale=scale, rows=[12])
+    assert np.max(np.abs(dense[0, 0, 0] - out[0, 0, 0])) > 1e-3
+
+
+def test_toy36_without_spread_sparse_equals_dense():
+    q, k, v, blk, scale = toy36(e_scale=0.0)
+    dense = oracle.dense(q, k[:, :0], v[:, :0], k, v, 0, scale=scale)
+    for alpha in (0.2, 0.1, 1.0):
+        out, _ = oracle.sparse(q, k, v, 0, blk, alpha, scale=scale)
+        assert np.max(np.abs(out - dense)) <= 1e-12
+
+
+def sparse_case(seed, N=80, s=16, Hq=4, Hkv=2, d=8):
+    g = np.random.default_rng(seed)
+    q = g.standard_normal((1, N, Hq, d))
+    k = g.standard_normal((1, s + N, Hkv, d))
+    v = g.standard_normal((1, s + N, Hkv, d))
+    return q, k, v, s
+
+
+def test_sparse_alpha_zero_equals_dense():
+    q, k, v, s = sparse_case(20)
+    dense = oracle.dense(q, k[:, :s], v[:, :s], k[:, s:], v[:, s:], s)
+    out, sel = oracle.sparse(q, k, v, s, 8, 0.0)
+    assert oracle.skip_share(sel) == 0.0
+    assert np.max(np.abs(out - dense)) <= 1e-12
+
+
+def test_sparse_block_constant_keys_equals_dense():
+    """Keys constant within each block make the pooled row exact: sparse == dense for every alpha."""
+    q, k, v, s = sparse_case(21)
+    blk = 8
+    T = k.shape[1]
+    for b0 in range(0, T, blk):
+        k[:, b0:b0 + blk] = k[:, b0:b0 + 1]
+    dense = oracle.dense(q, k[:, :s], v[:, :s], k[:, s:], v[:, s:], s)
+    for alpha in (0.05, 0.3, 0.9, 1.0):
+        out, sel = oracle.sparse(q, k, v, s, blk, alpha)
+        assert oracle.skip_share(sel) > 0.0
+        assert np.max(np.abs(out - dense)) <= 1e-12
+
+
+def test_sparse_single_block_equals_dense():
+    q, k, v, _ = sparse_case(22, N=7, s=0)
+    dense = oracle.dense(q, k[:, :0], v[:, :0], k, v, 0)
+    out, _ = oracle.sparse(q, k, v, 0, 8, 0.5)
+    assert np.max(np.abs(out - dense)) <= 1e-12
+
+
+def test_pool_blocks_against_prefix_sums():
+    g = np.random.default_rng(23)
+    x = g.standard_normal((2, 29, 3, 5))
+    pooled = oracle.pool_blocks(x, 8)
+    cs = np.concatenate([np.zeros((2, 1, 3, 5)), np.cumsum(x, axis=1)], axis=1)
+    for bk in range(4):
+        a, e = bk * 8, min(29, bk * 8 + 8)
+        assert np.allclose(pooled[:, :, bk], ((cs[:, e] - cs[:, a]) / (e - a)), atol=1e-13)
+    assert np.array_equal(oracle.block_counts(29, 8), [8, 8, 8, 5])
+
+
+def test_selection_nested_in_alpha():
+    q, k, v, s = sparse_case(24, N=120, s=40)
+    sels = [oracle.block_select(q, k, s, 8, a) for a in (1.0, 0.5, 0.1, 0.0)]
+    for lo, hi in zip(sels, sels[1:]):
+        assert np.all(~lo.kept | hi.kept)
+    # alpha = 1 keeps the diagonal plus the hottest candidate(s) only
+    sel = sels[0]
+    ob = (s + sel.rows) // 8
+    for r in range(len(sel.rows)):
+        for hi_ in range(q.shape[2]):
+            kept = set(np.flatnonzero(sel.kept[0, r, hi_]).tolist())
+            if ob[r] == 0:
+                assert kept == {0}
+            else:
+                best = int(np.argmax(sel.scores[0, r, hi_, :ob[r]]))
+                assert kept == {best, int(ob[r])}
+
+
+def test_sparse_negative_control():
+    """alpha 0.1 vs alpha 0 on planted data must differ by >= 10x the 5e-3 output tolerance."""
+    w = pi.planted_workload("tiny", 5, 1, 4, 2, 32, 1024, 1024, "bf16", block=64, beta=8.0)
+    q, k, v = w.f64(w.q), w.f64(w.k), w.f64(w.v)
+    rows = np.arange(512, 1024, 7)
+    a, sel = oracle.sparse(q, k, v, 0, 64, 0.1, rows=rows)
+    b, _ = oracle.sparse(q, k, v, 0, 64, 0.0, rows=rows)
+    assert oracle.skip_share(sel) > 0.5
+    assert np.max(np.abs(a - b)) > 10 * 5e-3
