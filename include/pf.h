@@ -1,0 +1,177 @@
+/*
+ * pf.h -- C ABI of libpf: long-context prefill attention on one GB300 (sm_103a).
+ *
+ * Three operations, each launched asynchronously on the caller's CUDA stream:
+ *
+ *   pf_attn_dense   a prompt chunk of queries attends to a token-major K/V
+ *                   history plus its own keys under an additive mask, and the
+ *                   chunk's K/V are re-emitted in cache layout.
+ *                   ("ANE Prefill Research", section "How the ANE prefill path
+ *                   works": chunk rows + token-major K/V history + additive
+ *                   mask in; attention output + the chunk's cache-layout K/V
+ *                   out; "Folding a sparse indexer's selection into the mask":
+ *                   dropped keys carry -30000 so exp() gives exactly zero.)
+ *   pf_block_index  mean-pools every key block, scores every query row
+ *                   against the pooled keys and keeps the local diagonal plus
+ *                   the blocks above alpha x the row's hottest block.
+ *                   ("Porting FlashPrefill V2 to Apple silicon for faster
+ *                   prefill", sections "Compress keys before the heavy work",
+ *                   "A cheap map of where the attention lives", "The
+ *                   algorithm starts here".)
+ *   pf_attn_sparse  exact attention over the kept blocks plus a pooled
+ *                   correction for the skipped ones (same page, section
+ *                   "Compute the peaks, summarize the rest"): a skipped block b
+ *                   adds n_b * exp(q . kbar_b * scale) to the softmax
+ *                   denominator and that weight times vbar_b to the numerator.
+ *
+ * Conventions shared by every entry point
+ *   - Positions are absolute: chunk row i is position start_pos + i; key j is
+ *     position j (history rows first, then the chunk's rows).
+ *   - Tensors are token-major with the head dimension d contiguous:
+ *       q                 [B, C, Hq, d]
+ *       k_hist, v_hist    [B, start_pos, Hkv, d]
+ *       k_chunk, v_chunk  [B, C, Hkv, d]
+ *       k, v (sparse)     [B, start_pos + C, Hkv, d]
+ *     Strides are given in ELEMENTS for the (batch, token, head) axes; a
+ *     stride triple of all zeros means "contiguous" for that tensor.
+ *   - GQA: query head h reads KV head h / (Hq / Hkv).
+ *   - Ownership: the caller allocates every buffer (device memory) and keeps it
+ *     alive until the stream reaches the call.  The library allocates nothing
+ *     per call and never synchronises the stream.
+ *   - Errors: arguments are validated synchronously before anything is
+ *     launched.  PF_EINVAL = bad pointer / shape / stride / alignment;
+ *     PF_EUNSUPPORTED = a valid request outside what the kernels implement
+ *     (they refuse rather than fall back); PF_ECUDA = a CUDA launch error.  A
+ *     device-side bounded wait that gave up is reported as PF_ETIMEOUT by
+ *     pf_stream_status().  pf_last_error() returns the calling thread's last
+ *     message.  Nothing is written when a call returns an error.
+ */
+#ifndef PF_H_
+#define PF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PF_OK = 0,
+  PF_EINVAL = 1,
+  PF_EUNSUPPORTED = 2,
+  PF_ECUDA = 3,
+  PF_ETIMEOUT = 4
+} pf_status;
+
+typedef enum { PF_F16 = 0, PF_BF16 = 1, PF_F32 = 2 } pf_dtype;
+
+/* Problem description shared by the three entry points. */
+typedef struct {
+  int32_t B;            /* batch */
+  int32_t Hq;           /* query heads */
+  int32_t Hkv;          /* KV heads; Hq % Hkv == 0 */
+  int32_t d;            /* head dim: 64 or 128 */
+  int32_t C;            /* query rows in this call (the chunk), >= 1 */
+  pf_dtype in_dtype;    /* q/k/v element type: PF_F16 or PF_BF16 */
+  pf_dtype out_dtype;   /* out element type: PF_F32, PF_BF16 or PF_F16 */
+  pf_dtype mask_dtype;  /* PF_F32 or PF_F16 (a bf16 mask cannot hold -30000 exactly) */
+  float scale;          /* logit scale; 0 means 1/sqrt(d) */
+  int64_t q_stride[3];  /* q over (b, t, h) */
+  int64_t kh_stride[3]; /* k_hist / v_hist over (b, t, h); sparse: k / v */
+  int64_t kc_stride[3]; /* k_chunk / v_chunk over (b, t, h) */
+  int64_t o_stride[3];  /* out over (b, t, h) */
+  int64_t okv_stride[3];/* out_k / out_v over (b, h, t); zeros = [B, Hkv, C, d] */
+  int64_t mask_ld;      /* elements between mask rows; 0 means start_pos + C */
+} pf_shape;
+
+/*
+ * Dense chunked prefill.
+ *   out[b, i, h, :] = sum_j w_j v_j / sum_j w_j,
+ *   w_j = exp(l_j - max_j l_j),  l_j = (q[b,i,h] . k_j) * scale + M[i, j],
+ * over all keys j < start_pos + C (k_j from k_hist for j < start_pos, else
+ * from k_chunk).  mask: additive [C, start_pos + C] (row stride mask_ld),
+ * shared by every batch and head; a key with -30000 contributes exactly zero
+ * to any row that has a key above -1e4.  mask == NULL means causal
+ * (M = 0 for j <= start_pos + i, else the key is excluded), the same result as
+ * the explicit 0 / -30000 causal mask.  With an explicit mask visibility is
+ * the mask alone.
+ * out_k / out_v (optional, both or neither): bit copies of k_chunk / v_chunk
+ * written at okv_stride, by default head-major [B, Hkv, C, d], so a caller can
+ * point them at row start_pos of its own cache.
+ * Requirements: start_pos % 128 == 0 (PF_EUNSUPPORTED otherwise); every base
+ * pointer 16-byte aligned and every stride a multiple of 16 bytes (PF_EINVAL);
+ * k_hist / v_hist may be NULL when start_pos == 0.
+ */
+pf_status pf_attn_dense(const pf_shape* shape, const void* q, const void* k_hist,
+                        const void* v_hist, const void* k_chunk, const void* v_chunk,
+                        const void* mask, int32_t start_pos, void* out, void* out_k,
+                        void* out_v, void* stream);
+
+/* Block selection produced by pf_block_index and consumed by pf_attn_sparse.
+ * nblk = ceil((start_pos + C) / block); nqt = ceil(C / 128); W = ceil(nblk / 32). */
+typedef struct {
+  uint32_t* row_bits;  /* [B, Hq, C, W]: bit (b % 32) of word b / 32 set iff the row keeps block b */
+  int32_t* tile_list;  /* [B, Hq, nqt, nblk]: ascending union of the kept blocks of the tile's rows */
+  int32_t* tile_cnt;   /* [B, Hq, nqt]: valid entries of tile_list */
+  float* kbar;         /* [B, Hkv, nblk, d]: pooled (mean) keys, fp32 */
+} pf_sel;
+
+/* Element counts of the pf_sel buffers and of the pf_attn_sparse workspace. */
+typedef struct {
+  int64_t nblk, nqt, words;
+  int64_t row_bits_elems, tile_list_elems, tile_cnt_elems, kbar_elems;
+  int64_t pooled_bytes; /* workspace bytes for pf_attn_sparse */
+} pf_sparse_sizes;
+
+pf_status pf_sparse_query_sizes(const pf_shape* shape, int32_t start_pos, int32_t block,
+                                pf_sparse_sizes* sizes);
+
+/*
+ * Block index.  For row i (p = start_pos + i) and head h: ob = p / block;
+ * candidates are the blocks b < ob; s_ib = (q_i . kbar_b) * scale with kbar_b
+ * the mean of block b's keys; candidate b is kept iff
+ * s_ib - max_c s_ic >= ln(alpha) (alpha = 0 keeps every candidate); the
+ * diagonal block ob is always kept.  q [B, C, Hq, d]; k [B, start_pos + C, Hkv, d]
+ * (history and chunk contiguous in one cache, strides kh_stride).
+ * Requirements: block == 128, 0 <= alpha <= 1, start_pos % 128 == 0.
+ */
+pf_status pf_block_index(const pf_shape* shape, const void* q, const void* k, int32_t start_pos,
+                         int32_t block, float alpha, const pf_sel* sel, void* stream);
+
+/*
+ * Block-sparse attention with pooled correction.  Row i (p = start_pos + i),
+ * head h, kept set K_i from sel (row_bits), skipped set R_i = {b < ob} \ K_i:
+ *   out = (sum_{j <= p, j/block in K_i} e^(l_j - m) v_j + sum_{b in R_i} n_b e^(s_ib - m) vbar_b)
+ *       / (sum_{j <= p, j/block in K_i} e^(l_j - m)     + sum_{b in R_i} n_b e^(s_ib - m)).
+ * pooled: caller-allocated workspace of pf_sparse_sizes.pooled_bytes; on
+ * return it starts with vbar, the fp32 block means of v, [B, Hkv, nblk, d];
+ * the rest is scratch.  sel must come from pf_block_index on the same q, k,
+ * start_pos and block.
+ */
+pf_status pf_attn_sparse(const pf_shape* shape, const void* q, const void* k, const void* v,
+                         int32_t start_pos, int32_t block, const pf_sel* sel, void* pooled,
+                         void* out, void* stream);
+
+/* Synchronise `stream`, then report (and clear) a device-side error: PF_ETIMEOUT
+ * if a bounded wait in a kernel gave up since the last check, PF_ECUDA on a CUDA
+ * error, else PF_OK. */
+pf_status pf_stream_status(void* stream);
+
+/* Bounded-wait limit in SM clock cycles (default 4e8, about 0.2 s). */
+void pf_set_wait_timeout(int64_t cycles);
+
+/* Test hook: nonzero makes the next attention launches withhold one MMA
+ * completion signal so that the consumers' bounded waits run out. */
+void pf_set_debug_withhold(int32_t on);
+
+/* Kernel launches issued by this thread since the counter was last reset. */
+int64_t pf_launch_count(int32_t reset);
+
+const char* pf_last_error(void);
+const char* pf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PF_H_ */

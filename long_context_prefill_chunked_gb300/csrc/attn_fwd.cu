@@ -1,0 +1,583 @@
+// Prefill attention forward for sm_103a: TMA-staged Q/K/V tiles, tcgen05 MMAs
+// accumulating S = Q K^T and O += P V in tensor memory, exp2 online softmax.
+//
+// Method: "Flash attention on ANE: fast long-context prefill", section "Flash
+// attention: the core insight" (tile Q and K/V, keep a running max and sum,
+// accumulate weighted V, never materialise the score matrix); the chunk +
+// history + additive-mask contract of "ANE Prefill Research", section "How the
+// ANE prefill path works"; and for MODE_SPARSE the kept-block walk plus pooled
+// correction of "Porting FlashPrefill V2 to Apple silicon for faster prefill",
+// section "Compute the peaks, summarize the rest".
+//
+// One CTA = one work unit = (batch b, query tile of 128 rows, `slots` query
+// heads of the same KV group).  The slots share every K/V tile (GQA): one TMA
+// load feeds both heads' MMAs.
+//   warps 0-3  softmax for slot 0 (thread t owns query row t = TMEM lane t)
+//   warps 4-7  softmax for slot 1
+//   warp  8    TMA producer (Q once, then K/V tiles through a 2-stage ring)
+//   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
+//   warps 10-11 spare (they complete the third warpgroup for setmaxnreg)
+// Tensor memory (512 columns): slot s uses columns [256s, 256s+128) for S (P
+// is written back over its first half as 16-bit pairs) and [256s+128,
+// 256s+128+d) for the fp32 O accumulator.
+// MMA order per key tile j: PV(slot0, j), S(slot0, j+1), PV(slot1, j),
+// S(slot1, j+1); each softmax group works on its tile while the tensor core
+// runs the other slot's pair.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace pf {
+namespace {
+
+constexpr int NST = 2;                               // K/V ring stages
+constexpr uint32_t SM_Q = 0;                         // slot s: +32 KB * s (two 64-column boxes)
+constexpr uint32_t SM_K = 65536;                     // stage st: +32 KB * st
+constexpr uint32_t SM_V = SM_K + NST * 32768;
+constexpr uint32_t SM_BAR = SM_V + NST * 32768;      // mbarriers, TMEM address, abort flag
+constexpr uint32_t SM_SEQ = SM_BAR + 256;            // sparse: merged key-block sequence
+constexpr int kMaxBlocks = 2048;                     // sparse: key blocks per sequence (256K keys)
+constexpr uint32_t SM_BM = SM_SEQ + kMaxBlocks * 4;  // sparse: union bitmap
+constexpr uint32_t SM_BYTES = SM_BM + kMaxBlocks / 8 + 16;
+constexpr uint32_t SM_ALLOC = SM_BYTES + 1024;       // slack for 1024-byte alignment
+
+enum {
+  B_Q = 0,
+  B_KF = 1,             // K tile landed, per stage
+  B_VF = B_KF + NST,    // V tile landed, per stage
+  B_KE = B_VF + NST,    // stage free again (both slots' MMAs on it done)
+  B_SF = B_KE + NST,    // S ready, per slot
+  B_PF = B_SF + 2,      // P written (and O rescaled), per slot
+  B_OF = B_PF + 2,      // last PV done
+  B_DR = B_OF + 1,      // drain: all issued MMAs done
+  N_BARS = B_DR + 1
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+// Lazy rescale: a row keeps its stale running max while the new tile's max
+// exceeds it by at most 8 (log2 units), so P <= 256; the final O / l uses the
+// same max for numerator and denominator, so the result is unchanged.
+constexpr float kRescaleThreshold = 8.0f;
+
+// where-codes recorded with a timeout: (role << 8) | barrier
+enum { R_PROD = 1, R_MMA = 2, R_SOFT = 3 };
+
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, long long timeout,
+                                         volatile int* abort_flag, unsigned* status,
+                                         unsigned where) {
+  bool ok = mbar_wait(bar, parity, timeout, abort_flag, status, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used only while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long timeout,
+                                           unsigned* status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > timeout) {
+      record_error(status, ST_TIMEOUT, 0xFFu);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void ld_row128(uint32_t taddr, float (&x)[128]) {
+  uint32_t r[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    tmem_ld32(taddr + 32 * q, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[32 * q + i] = __uint_as_float(r[i]);
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = sb + SM_BAR;
+#define BAR(i) (bar0 + 8u * (uint32_t)(i))
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_BAR + 8 * N_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_BAR + 8 * N_BARS + 4);
+  int* n_ex_slot = reinterpret_cast<int*>(smem + SM_BAR + 8 * N_BARS + 8);
+  int* seq = reinterpret_cast<int*>(smem + SM_SEQ);
+
+  // ---- work unit: heaviest query tiles first (longest causal key range)
+  const int per_qt = a.n_hp * a.B;
+  const int qt = a.n_qt - 1 - (int)blockIdx.x / per_qt;
+  const int rem = (int)blockIdx.x % per_qt;
+  const int b = rem / a.n_hp;
+  const int h0 = (rem % a.n_hp) * a.slots;
+  const int g = h0 / a.G;
+  const int q0 = qt * kTile;
+  const int ob = (a.s + q0) / kTile;  // key block holding this tile's diagonal
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(B_Q), 1);
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(BAR(B_KF + st), 1);
+      mbar_init(BAR(B_VF + st), 1);
+      mbar_init(BAR(B_KE + st), 1);
+    }
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(BAR(B_SF + sl), 1);
+      mbar_init(BAR(B_PF + sl), 4);
+    }
+    mbar_init(BAR(B_OF), 1);
+    mbar_init(BAR(B_DR), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (MODE == MODE_SPARSE && warp == 8) {
+    // Union of the slots' kept-block lists, ascending, via a bitmap.
+    uint32_t* bm = reinterpret_cast<uint32_t*>(smem + SM_BM);
+    const long long t0 = (long long)(b * a.Hq + h0) * a.n_qt + qt;
+    const int32_t* l0 = a.tile_list + t0 * a.nblk;
+    const int c0 = min(max(a.tile_cnt[t0], 0), a.nblk);
+    const int c1 = (a.slots == 2) ? min(max(a.tile_cnt[t0 + a.n_qt], 0), a.nblk) : 0;
+    const int32_t* l1 = l0 + (long long)a.n_qt * a.nblk;
+    for (int w = lane; w < a.words; w += 32) bm[w] = 0u;
+    __syncwarp();
+    for (int i = lane; i < c0; i += 32) {
+      const int kb = l0[i];
+      if (kb >= 0 && kb < a.nblk) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
+    }
+    for (int i = lane; i < c1; i += 32) {
+      const int kb = l1[i];
+      if (kb >= 0 && kb < a.nblk) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
+    }
+    __syncwarp();
+    int base = 0;
+    for (int w0 = 0; w0 < a.words; w0 += 32) {
+      const int w = w0 + lane;
+      const uint32_t bits = (w < a.words) ? bm[w] : 0u;
+      const int cnt = __popc(bits);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int pos = base + incl - cnt;
+      uint32_t rb = bits;
+      while (rb) {
+        const int t = __ffs(rb) - 1;
+        rb &= rb - 1u;
+        seq[pos++] = w * 32 + t;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) *n_ex_slot = base;
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int n_pool = 0, n_tiles;
+  if (MODE == MODE_CAUSAL) {
+    n_tiles = ob + 1;
+  } else if (MODE == MODE_MASK) {
+    n_tiles = (a.T + kTile - 1) / kTile;
+  } else {
+    n_pool = (ob + kTile - 1) / kTile;
+    n_tiles = n_pool + *n_ex_slot;
+  }
+
+  // 384 threads x 168 registers at launch; the softmax warpgroups take 232,
+  // the producer/MMA warpgroup keeps 40: 2*128*232 + 128*40 = 384*168.
+  if (warp >= 8) {
+    regs_dec<40>();
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int nd = a.d / 64;
+      const uint32_t tile_bytes = (uint32_t)nd * 16384u;
+      int last_use[NST];
+      for (int st = 0; st < NST; ++st) last_use[st] = -1;
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.kh);
+      tma_prefetch_desc(&maps.vh);
+      mbar_arrive_expect_tx(BAR(B_Q), tile_bytes * (uint32_t)a.slots);
+      for (int sl = 0; sl < a.slots; ++sl)
+        for (int c = 0; c < nd; ++c)
+          tma_load_4d(sb + SM_Q + 32768u * sl + 16384u * c, &maps.q, BAR(B_Q), 64 * c, h0 + sl,
+                      q0, b);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % NST, use = j / NST;
+        if (use > 0 && !mbar_wait(BAR(B_KE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
+                                  (R_PROD << 8) | (B_KE + st)))
+          break;
+        const CUtensorMap *mk, *mv;
+        int c1, c2;
+        if (MODE == MODE_SPARSE && j < n_pool) {
+          mk = &maps.kbar;  // pooled keys [B, Hkv, nblk, d]: rows = pooled blocks
+          mv = &maps.vbar;
+          c1 = j * kTile;
+          c2 = g;
+        } else {
+          const int kt = (MODE == MODE_SPARSE) ? seq[j - n_pool] : j;
+          if (kt < a.n_hist_tiles) {
+            mk = &maps.kh;
+            mv = &maps.vh;
+            c2 = kt * kTile;
+          } else {
+            mk = &maps.kc;
+            mv = &maps.vc;
+            c2 = kt * kTile - a.s;
+          }
+          c1 = g;
+        }
+        mbar_arrive_expect_tx(BAR(B_KF + st), tile_bytes);
+        for (int c = 0; c < nd; ++c)
+          tma_load_4d(sb + SM_K + 32768u * st + 16384u * c, mk, BAR(B_KF + st), 64 * c, c1, c2, b);
+        mbar_arrive_expect_tx(BAR(B_VF + st), tile_bytes);
+        for (int c = 0; c < nd; ++c)
+          tma_load_4d(sb + SM_V + 32768u * st + 16384u * c, mv, BAR(B_VF + st), 64 * c, c1, c2, b);
+        last_use[st] = use;
+      }
+      if (*abort_flag) {  // let this warp's copies land before the CTA exits
+        drain_wait(BAR(B_Q), 0, a.timeout, a.status);
+        for (int st = 0; st < NST; ++st)
+          if (last_use[st] >= 0) {
+            drain_wait(BAR(B_KF + st), last_use[st] & 1, a.timeout, a.status);
+            drain_wait(BAR(B_VF + st), last_use[st] & 1, a.timeout, a.status);
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = make_idesc_f16((uint32_t)a.ab_type, 128, 128, 0);
+      const uint32_t idesc_pv = make_idesc_f16((uint32_t)a.ab_type, 128, (uint32_t)a.d, 1);
+      const int kq = a.d / 16;
+      auto issue_qk = [&](int sl, int st) {
+        const uint32_t d_tmem = tmem + 256u * sl;
+#pragma unroll 1
+        for (int kk = 0; kk < kq; ++kk) {
+          const uint32_t off = 16384u * (kk >> 2) + 32u * (kk & 3);
+          const uint64_t ad = make_sdesc_sw128(sb + SM_Q + 32768u * sl + off, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(sb + SM_K + 32768u * st + off, 16, 1024);
+          mma_ss(d_tmem, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int sl, int st, bool acc) {
+        const uint32_t d_tmem = tmem + 256u * sl + 128u;
+#pragma unroll 1
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t bd = make_sdesc_sw128(sb + SM_V + 32768u * st + 2048u * kk, 16384, 1024);
+          mma_ts(d_tmem, tmem + 256u * sl + 8u * kk, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(BAR(B_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | B_Q);
+      tc_fence_after();
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % NST;
+        const uint32_t ph = (uint32_t)(j / NST) & 1u;
+        if (j == 0) {
+          ok = mbar_wait(BAR(B_KF + st), ph, a.timeout, abort_flag, a.status, (R_MMA << 8) | (B_KF + st));
+          if (!ok) break;
+          tc_fence_after();
+          for (int sl = 0; sl < a.slots; ++sl) {
+            issue_qk(sl, st);
+            if (!a.withhold) tc_commit(BAR(B_SF + sl));
+          }
+        }
+        ok = mbar_wait(BAR(B_VF + st), ph, a.timeout, abort_flag, a.status, (R_MMA << 8) | (B_VF + st));
+        if (!ok) break;
+        tc_fence_after();
+        for (int sl = 0; sl < a.slots; ++sl) {
+          ok = mbar_wait(BAR(B_PF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
+                         (R_MMA << 8) | (B_PF + sl));
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(sl, st, j > 0);
+          if (j + 1 < n_tiles) {
+            const int st1 = (j + 1) % NST;
+            if (sl == 0) {
+              ok = mbar_wait(BAR(B_KF + st1), (uint32_t)((j + 1) / NST) & 1u, a.timeout,
+                             abort_flag, a.status, (R_MMA << 8) | (B_KF + st1));
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_qk(sl, st1);
+            tc_commit(BAR(B_SF + sl));
+          }
+        }
+        if (!ok) break;
+        tc_commit(BAR(B_KE + st));
+      }
+      if (ok) tc_commit(BAR(B_OF));
+      tc_commit(BAR(B_DR));  // no MMA may still run when tensor memory is released
+      drain_wait(BAR(B_DR), 0, a.timeout, a.status);
+    }
+    __syncwarp();
+  }
+  } else {
+    regs_inc<232>();
+  if ((warp >> 2) < a.slots) {
+    // ------------------------------------------------------------ softmax
+    const int sl = warp >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t t_s = tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl;
+    const uint32_t t_o = t_s + 128u;
+    const int h = h0 + sl;
+    const int row = q0 + r;
+    const bool valid = row < a.C;
+    const uint32_t* bits_row = nullptr;
+    if (MODE == MODE_SPARSE && valid)
+      bits_row = a.row_bits + ((long long)(b * a.Hq + h) * a.C + row) * a.words;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = wait_all(BAR(B_SF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
+                    (R_SOFT << 8) | (B_SF + sl));
+      if (!ok) break;
+      tc_fence_after();
+      float x[128];
+      ld_row128(t_s, x);
+      float xs = a.scale_log2, bias = 0.f;
+      if (MODE == MODE_CAUSAL) {
+        if (j == n_tiles - 1) {  // diagonal tile: key q0 + c visible iff c <= r
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > r) x[c] = -INFINITY;
+        }
+      } else if (MODE == MODE_MASK) {
+        xs = 1.f;
+        const int key0 = j * kTile;
+        if (valid && a.mask_vec && key0 + kTile <= a.T) {
+          if (a.mask_f16) {
+            const uint4* mp = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const __half*>(a.mask) + (long long)row * a.mask_ld + key0);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+              const uint4 w = __ldg(mp + v);
+              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+                x[8 * v + 2 * e] = fmaf(x[8 * v + 2 * e], a.scale_log2, f.x * kLog2e);
+                x[8 * v + 2 * e + 1] = fmaf(x[8 * v + 2 * e + 1], a.scale_log2, f.y * kLog2e);
+              }
+            }
+          } else {
+            const float4* mp = reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(a.mask) + (long long)row * a.mask_ld + key0);
+#pragma unroll
+            for (int v = 0; v < 32; ++v) {
+              const float4 w = __ldg(mp + v);
+              x[4 * v + 0] = fmaf(x[4 * v + 0], a.scale_log2, w.x * kLog2e);
+              x[4 * v + 1] = fmaf(x[4 * v + 1], a.scale_log2, w.y * kLog2e);
+              x[4 * v + 2] = fmaf(x[4 * v + 2], a.scale_log2, w.z * kLog2e);
+              x[4 * v + 3] = fmaf(x[4 * v + 3], a.scale_log2, w.w * kLog2e);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int key = key0 + c;
+            float mv = 0.f;
+            if (valid && key < a.T) {
+              const long long o = (long long)row * a.mask_ld + key;
+              mv = a.mask_f16 ? __half2float(reinterpret_cast<const __half*>(a.mask)[o])
+                              : reinterpret_cast<const float*>(a.mask)[o];
+            }
+            x[c] = (key < a.T) ? fmaf(x[c], a.scale_log2, mv * kLog2e) : -INFINITY;
+          }
+        }
+      } else {  // MODE_SPARSE
+        if (j < n_pool) {
+          // pooled keys: column c is block j*128 + c; a row takes it iff the
+          // block is an earlier candidate (< ob) that the row did not keep
+          bias = a.log2_nb;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int wi = j * 4 + q;
+            const uint32_t w = (bits_row != nullptr && wi < a.words) ? __ldg(bits_row + wi) : 0u;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int blk = wi * 32 + i;
+              if (blk >= ob || ((w >> i) & 1u)) x[32 * q + i] = -INFINITY;
+            }
+          }
+        } else {
+          const int kb = seq[j - n_pool];
+          if (kb == ob) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > r) x[c] = -INFINITY;
+          } else {
+            const bool keep =
+                bits_row == nullptr || ((__ldg(bits_row + (kb >> 5)) >> (kb & 31)) & 1u);
+            if (!keep) {
+#pragma unroll
+              for (int c = 0; c < 128; ++c) x[c] = -INFINITY;
+            }
+          }
+        }
+      }
+      // ---- online softmax (log2 domain)
+      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, x[c]);
+        mx1 = fmaxf(mx1, x[c + 1]);
+        mx2 = fmaxf(mx2, x[c + 2]);
+        mx3 = fmaxf(mx3, x[c + 3]);
+      }
+      const float mraw = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float mt = (mraw == -INFINITY) ? -INFINITY : fmaf(mraw, xs, bias);
+      const bool need = mt > m + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float mn = fmaxf(m, mt);
+        const float f = (m == -INFINITY) ? 0.f : ex2(m - mn);
+        l *= f;
+        if (j > 0) {
+          uint32_t o[32];
+          for (int c0 = 0; c0 < a.d; c0 += 32) {
+            tmem_ld32(t_o + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(t_o + c0, o);
+          }
+        }
+        m = mn;
+      }
+      const float off = bias - ((m == -INFINITY) ? 0.f : m);
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(x[32 * q + 2 * i], xs, off));
+          const float p1 = ex2(fmaf(x[32 * q + 2 * i + 1], xs, off));
+          ls0 += p0;
+          ls1 += p1;
+          pk[i] = a.ab_type ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+        }
+        tmem_st16(t_s + 16u * q, pk);
+      }
+      l += ls0 + ls1;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_PF + sl));
+    }
+    // ---- epilogue: out = O / l
+    if (ok)
+      ok = wait_all(BAR(B_OF), 0, a.timeout, abort_flag, a.status, (R_SOFT << 8) | B_OF);
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const long long obase = (long long)b * a.o_sb + (long long)row * a.o_st + (long long)h * a.o_sh;
+      for (int c0 = 0; c0 < a.d; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c0, o);
+        tmem_wait_ld();
+        if (valid) {
+          if (a.out_dtype == 2) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + obase + c0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                   __uint_as_float(o[4 * v + 2]) * inv,
+                                   __uint_as_float(o[4 * v + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + obase + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float lo = __uint_as_float(o[8 * v + 2 * e]) * inv;
+                const float hi = __uint_as_float(o[8 * v + 2 * e + 1]) * inv;
+                w[e] = (a.out_dtype == 1) ? pack_bf16(lo, hi) : pack_f16(lo, hi);
+              }
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+#undef BAR
+}
+
+__global__ void kv_relayout_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                   int B, int C, int H, int d, long long s0, long long s1,
+                                   long long s2, long long d0, long long d1, long long d2) {
+  const int nv = d / 8;
+  const long long total = (long long)B * C * H * nv;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int v = (int)(i % nv);
+    long long rest = i / nv;
+    const int h = (int)(rest % H);
+    rest /= H;
+    const int t = (int)(rest % C);
+    const int b = (int)(rest / C);
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src + b * s0 + t * s1 + h * s2) + v);
+    reinterpret_cast<uint4*>(dst + b * d0 + h * d1 + t * d2)[v] = w;
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const AttnMaps& maps, const AttnArgs& a, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SM_ALLOC);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = a.n_qt * a.n_hp * a.B;
+  attn_fwd_kernel<MODE><<<grid, kAttnThreads, SM_ALLOC, st>>>(maps, a);
+  ++t_launches;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaStream_t st) {
+  switch (mode) {
+    case MODE_CAUSAL: return launch_mode<MODE_CAUSAL>(maps, a, st);
+    case MODE_MASK: return launch_mode<MODE_MASK>(maps, a, st);
+    default: return launch_mode<MODE_SPARSE>(maps, a, st);
+  }
+}
+
+cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, int d,
+                               const long long ss[3], const long long ds[3], cudaStream_t st) {
+  const long long total = (long long)B * C * H * (d / 8);
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int grid = (int)(want < 152 * 16 ? want : 152 * 16);
+  kv_relayout_kernel<<<grid, threads, 0, st>>>(static_cast<const uint16_t*>(src),
+                                               static_cast<uint16_t*>(dst), B, C, H, d, ss[0],
+                                               ss[1], ss[2], ds[0], ds[1], ds[2]);
+  ++t_launches;
+  return cudaGetLastError();
+}
+
+}  // namespace pf

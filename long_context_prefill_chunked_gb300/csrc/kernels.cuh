@@ -1,0 +1,81 @@
+// Internal kernel arguments and launchers of libpf (not part of the C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pf {
+
+constexpr int kTile = 128;        // query rows and keys per tile (= key block of the sparse path)
+constexpr int kAttnThreads = 384; // 8 softmax warps (2 slots x 4), TMA warp, MMA warp, 2 spare
+
+enum AttnMode : int { MODE_CAUSAL = 0, MODE_MASK = 1, MODE_SPARSE = 2 };
+
+struct AttnArgs {
+  int B, Hq, Hkv, G, d, C, s, T;
+  int n_qt;             // query tiles per (b, head)
+  int slots;            // query heads per CTA sharing one K/V stream (1 or 2)
+  int n_hp;             // head groups of `slots` heads per batch
+  int n_hist_tiles;     // key tiles served by the history map (s / 128)
+  int ab_type;          // 0 = f16, 1 = bf16 operands
+  float scale_log2;     // scale * log2(e)
+  // explicit additive mask (MODE_MASK)
+  const void* mask;
+  int mask_f16;         // 1 = fp16 mask, 0 = fp32
+  int mask_vec;         // rows 16-byte aligned: vector loads allowed
+  long long mask_ld;    // elements between mask rows
+  // output
+  void* out;
+  int out_dtype;        // 0 f16, 1 bf16, 2 f32
+  long long o_sb, o_st, o_sh;
+  // block-sparse selection (MODE_SPARSE)
+  const uint32_t* row_bits;   // [B, Hq, C, W]
+  const int32_t* tile_list;   // [B, Hq, n_qt, nblk]
+  const int32_t* tile_cnt;    // [B, Hq, n_qt]
+  int words, nblk;
+  float log2_nb;              // log2 of the pooled weight n_b (block size)
+  // robustness
+  unsigned* status;     // device status words (timeout flag, where)
+  long long timeout;    // bounded-wait limit, SM cycles
+  int withhold;         // test hook: never signal the first S tile
+};
+
+struct AttnMaps {
+  CUtensorMap q, kh, kc, vh, vc, kbar, vbar;
+};
+
+cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaStream_t st);
+
+// bit copy of the chunk's K (or V) into the cache layout
+cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, int d,
+                               const long long src_stride[3], const long long dst_stride[3],
+                               cudaStream_t st);
+
+// mean-pool each key block: x [B, T, H, d] -> fp32 [B, H, nblk, d] (+ optional 16-bit copy)
+struct PoolArgs {
+  const void* x;
+  int B, T, H, d, block, nblk;
+  long long sb, st, sh;
+  float* out_f32;        // [B, H, nblk, d]
+  void* out_lp;          // [B, H, nblk, d] in the input type, may be null
+};
+cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st);
+cudaError_t launch_f32_to_lp(const float* src, void* dst, long long n, int bf16, cudaStream_t st);
+
+struct IndexArgs {
+  const void* q;
+  int ab_type;
+  int B, Hq, Hkv, G, d, C, s, nblk, n_qt, words;
+  long long q_sb, q_st, q_sh;
+  const float* kbar;     // [B, Hkv, nblk, d]
+  float scale;
+  float log_alpha;       // ln(alpha); -inf when alpha == 0
+  uint32_t* row_bits;
+  int32_t* tile_list;
+  int32_t* tile_cnt;
+};
+cudaError_t launch_index(const IndexArgs& a, cudaStream_t st);
+
+extern thread_local long long t_launches;
+
+}  // namespace pf

@@ -1,0 +1,437 @@
+// C ABI of libpf: argument validation, TMA descriptor encoding and launches.
+// The operations and their contracts are documented in include/pf.h.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <string>
+
+#include "kernels.cuh"
+#include "pf.h"
+
+namespace pf {
+thread_local long long t_launches = 0;
+}  // namespace pf
+
+// Device status words written by the kernels' bounded waits: [0] flags, [1] where.
+static __device__ unsigned int g_status[2];
+
+using namespace pf;
+
+namespace {
+
+thread_local std::string t_err;
+long long g_timeout = 400000000LL;  // ~0.2 s at 2 GHz; legitimate waits take microseconds
+int g_withhold = 0;
+
+pf_status fail(pf_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+pf_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PF_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device address of g_status on the current device (looked up once per device).
+unsigned* status_words() {
+  static unsigned* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned*>(p);
+  }
+  return addr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int esize(pf_dtype t) { return t == PF_F32 ? 4 : 2; }
+
+// Fill a (b, t, h) element-stride triple; zeros mean contiguous [B, T, H, d].
+void strides_or_default(const int64_t in[3], int64_t T, int64_t H, int64_t d, long long out[3]) {
+  if (in[0] == 0 && in[1] == 0 && in[2] == 0) {
+    out[0] = T * H * d;
+    out[1] = H * d;
+    out[2] = d;
+  } else {
+    out[0] = in[0];
+    out[1] = in[1];
+    out[2] = in[2];
+  }
+}
+
+bool strides_ok(const long long s[3], int es) {
+  for (int i = 0; i < 3; ++i)
+    if (s[i] < 0 || ((s[i] * es) & 15) != 0) return false;
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 4-D tiled map over a 16-bit tensor with element strides (s1, s2, s3) for
+// dims 1..3 (dim 0 = d, contiguous); box = 64 elements x box1 x box2 x 1,
+// 128-byte swizzle, zero fill out of bounds.
+pf_status make_map(CUtensorMap* m, const void* base, pf_dtype dt, uint64_t d0, uint64_t d1,
+                   uint64_t d2, uint64_t d3, long long s1, long long s2, long long s3,
+                   uint32_t box1, uint32_t box2, const char* what) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(PF_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[4] = {d0, d1, d2, d3};
+  const cuuint64_t strides[3] = {(cuuint64_t)s1 * 2, (cuuint64_t)s2 * 2, (cuuint64_t)s3 * 2};
+  const cuuint32_t box[4] = {64, box1, box2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t =
+      dt == PF_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(m, t, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PF_ECUDA, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return PF_OK;
+}
+
+// Token-major tensor [B, T, H, d] -> map dims (d, H, T, B), box 64 x 1 x 128.
+pf_status map_tokens(CUtensorMap* m, const void* base, pf_dtype dt, int B, int T, int H, int d,
+                     const long long s[3], const char* what) {
+  return make_map(m, base, dt, d, H, T, B, s[2], s[1], s[0], 1, 128, what);
+}
+
+pf_status check_common(const pf_shape* sh, int32_t start_pos) {
+  if (sh == nullptr) return fail(PF_EINVAL, "shape is NULL");
+  if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->C < 1)
+    return fail(PF_EINVAL, "B, Hq, Hkv and C must be >= 1 (got %d, %d, %d, %d)", sh->B, sh->Hq,
+                sh->Hkv, sh->C);
+  if (sh->Hq % sh->Hkv != 0) return fail(PF_EINVAL, "Hq (%d) must be a multiple of Hkv (%d)", sh->Hq, sh->Hkv);
+  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  if (sh->in_dtype != PF_F16 && sh->in_dtype != PF_BF16)
+    return fail(PF_EUNSUPPORTED, "q/k/v dtype must be f16 or bf16");
+  if (sh->out_dtype != PF_F32 && sh->out_dtype != PF_BF16 && sh->out_dtype != PF_F16)
+    return fail(PF_EINVAL, "bad out dtype");
+  if (start_pos < 0) return fail(PF_EINVAL, "start_pos %d < 0", start_pos);
+  if (start_pos % kTile != 0)
+    return fail(PF_EUNSUPPORTED, "start_pos %d is not a multiple of %d", start_pos, kTile);
+  if ((long long)start_pos + sh->C > (1LL << 30)) return fail(PF_EINVAL, "sequence too long");
+  if (!(sh->scale >= 0.f) || isinf(sh->scale)) return fail(PF_EINVAL, "bad scale");
+  return PF_OK;
+}
+
+void fill_attn_common(const pf_shape* sh, int32_t start_pos, AttnArgs& a) {
+  a.B = sh->B;
+  a.Hq = sh->Hq;
+  a.Hkv = sh->Hkv;
+  a.G = sh->Hq / sh->Hkv;
+  a.d = sh->d;
+  a.C = sh->C;
+  a.s = start_pos;
+  a.T = start_pos + sh->C;
+  a.n_qt = (sh->C + kTile - 1) / kTile;
+  a.slots = (a.G % 2 == 0) ? 2 : 1;
+  a.n_hp = sh->Hq / a.slots;
+  a.ab_type = sh->in_dtype == PF_BF16 ? 1 : 0;
+  const float scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)sh->d);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out_dtype = sh->out_dtype == PF_F32 ? 2 : (sh->out_dtype == PF_BF16 ? 1 : 0);
+  a.timeout = g_timeout;
+  a.withhold = g_withhold;
+  a.status = status_words();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pf_last_error(void) { return t_err.c_str(); }
+
+const char* pf_version(void) { return "libpf 0.1 sm_103a"; }
+
+void pf_set_wait_timeout(int64_t cycles) { g_timeout = cycles > 1000 ? cycles : 1000; }
+
+void pf_set_debug_withhold(int32_t on) { g_withhold = on ? 1 : 0; }
+
+int64_t pf_launch_count(int32_t reset) {
+  const long long n = t_launches;
+  if (reset) t_launches = 0;
+  return n;
+}
+
+pf_status pf_stream_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned w[2] = {0, 0};
+  e = cudaMemcpyFromSymbol(w, g_status, sizeof(w));
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  if (w[0] == 0) return PF_OK;
+  const unsigned zero[2] = {0, 0};
+  cudaMemcpyToSymbol(g_status, zero, sizeof(zero));
+  return fail(PF_ETIMEOUT, "a bounded device wait gave up (status 0x%x, role %u, barrier %u)", w[0],
+              w[1] >> 8, w[1] & 0xFFu);
+}
+
+pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, const void* v_hist,
+                        const void* k_chunk, const void* v_chunk, const void* mask,
+                        int32_t start_pos, void* out, void* out_k, void* out_v, void* stream) {
+  pf_status rc = check_common(sh, start_pos);
+  if (rc != PF_OK) return rc;
+  if (q == nullptr || k_chunk == nullptr || v_chunk == nullptr || out == nullptr)
+    return fail(PF_EINVAL, "q, k_chunk, v_chunk and out must not be NULL");
+  if (start_pos > 0 && (k_hist == nullptr || v_hist == nullptr))
+    return fail(PF_EINVAL, "k_hist and v_hist are required when start_pos > 0");
+  if ((out_k == nullptr) != (out_v == nullptr)) return fail(PF_EINVAL, "give both out_k and out_v, or neither");
+  if (mask != nullptr && sh->mask_dtype != PF_F32 && sh->mask_dtype != PF_F16)
+    return fail(PF_EUNSUPPORTED, "mask dtype must be f32 or f16 (bf16 cannot hold -30000 exactly)");
+  const void* ptrs[] = {q, k_hist, v_hist, k_chunk, v_chunk, out, out_k, out_v};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return fail(PF_EINVAL, "every base pointer must be 16-byte aligned");
+  const int B = sh->B, C = sh->C, Hq = sh->Hq, Hkv = sh->Hkv, d = sh->d, s = start_pos;
+  long long qs[3], khs[3], kcs[3], os[3], okv[3];
+  strides_or_default(sh->q_stride, C, Hq, d, qs);
+  strides_or_default(sh->kh_stride, s, Hkv, d, khs);
+  strides_or_default(sh->kc_stride, C, Hkv, d, kcs);
+  strides_or_default(sh->o_stride, C, Hq, d, os);
+  if (sh->okv_stride[0] == 0 && sh->okv_stride[1] == 0 && sh->okv_stride[2] == 0) {
+    okv[0] = (long long)Hkv * C * d;
+    okv[1] = (long long)C * d;
+    okv[2] = d;
+  } else {
+    for (int i = 0; i < 3; ++i) okv[i] = sh->okv_stride[i];
+  }
+  if (!strides_ok(qs, 2) || !strides_ok(khs, 2) || !strides_ok(kcs, 2) || !strides_ok(okv, 2))
+    return fail(PF_EINVAL, "q/k/v strides must be non-negative multiples of 16 bytes");
+  if (!strides_ok(os, esize(sh->out_dtype))) return fail(PF_EINVAL, "out strides must be multiples of 16 bytes");
+
+  AttnArgs a{};
+  fill_attn_common(sh, start_pos, a);
+  a.n_hist_tiles = s / kTile;
+  a.out = out;
+  a.o_sb = os[0];
+  a.o_st = os[1];
+  a.o_sh = os[2];
+  int mode = MODE_CAUSAL;
+  if (mask != nullptr) {
+    mode = MODE_MASK;
+    a.mask = mask;
+    a.mask_f16 = sh->mask_dtype == PF_F16 ? 1 : 0;
+    a.mask_ld = sh->mask_ld > 0 ? sh->mask_ld : (long long)s + C;
+    if (a.mask_ld < (long long)s + C) return fail(PF_EINVAL, "mask_ld %lld < start_pos + C", a.mask_ld);
+    const int mes = a.mask_f16 ? 2 : 4;
+    a.mask_vec = (aligned16(mask) && ((a.mask_ld * mes) & 15) == 0) ? 1 : 0;
+  }
+
+  AttnMaps maps;
+  const pf_dtype dt = sh->in_dtype;
+  if ((rc = map_tokens(&maps.q, q, dt, B, C, Hq, d, qs, "q")) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.kc, k_chunk, dt, B, C, Hkv, d, kcs, "k_chunk")) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.vc, v_chunk, dt, B, C, Hkv, d, kcs, "v_chunk")) != PF_OK) return rc;
+  if (s > 0) {
+    if ((rc = map_tokens(&maps.kh, k_hist, dt, B, s, Hkv, d, khs, "k_hist")) != PF_OK) return rc;
+    if ((rc = map_tokens(&maps.vh, v_hist, dt, B, s, Hkv, d, khs, "v_hist")) != PF_OK) return rc;
+  } else {
+    maps.kh = maps.kc;
+    maps.vh = maps.vc;
+  }
+  maps.kbar = maps.kc;
+  maps.vbar = maps.vc;
+
+  if (a.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_attn(maps, a, mode, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (out_k != nullptr) {
+    if ((e = launch_kv_relayout(k_chunk, out_k, B, C, Hkv, d, kcs, okv, st)) != cudaSuccess)
+      return cuda_fail(e, "out_k copy");
+    if ((e = launch_kv_relayout(v_chunk, out_v, B, C, Hkv, d, kcs, okv, st)) != cudaSuccess)
+      return cuda_fail(e, "out_v copy");
+  }
+  return PF_OK;
+}
+
+pf_status pf_sparse_query_sizes(const pf_shape* sh, int32_t start_pos, int32_t block,
+                                pf_sparse_sizes* z) {
+  if (sh == nullptr || z == nullptr) return fail(PF_EINVAL, "NULL argument");
+  if (block != kTile) return fail(PF_EUNSUPPORTED, "block %d (supported: %d)", block, kTile);
+  const long long T = (long long)start_pos + sh->C;
+  z->nblk = (T + block - 1) / block;
+  z->nqt = (sh->C + kTile - 1) / kTile;
+  z->words = (z->nblk + 31) / 32;
+  z->row_bits_elems = (long long)sh->B * sh->Hq * sh->C * z->words;
+  z->tile_list_elems = (long long)sh->B * sh->Hq * z->nqt * z->nblk;
+  z->tile_cnt_elems = (long long)sh->B * sh->Hq * z->nqt;
+  z->kbar_elems = (long long)sh->B * sh->Hkv * z->nblk * sh->d;
+  const long long f32b = (z->kbar_elems * 4 + 255) / 256 * 256;
+  const long long lpb = (z->kbar_elems * 2 + 255) / 256 * 256;
+  z->pooled_bytes = f32b + 2 * lpb;
+  return PF_OK;
+}
+
+namespace {
+
+pf_status check_sparse(const pf_shape* sh, int32_t start_pos, int32_t block, long long ks[3],
+                       long long qs[3], pf_sparse_sizes* z) {
+  pf_status rc = check_common(sh, start_pos);
+  if (rc != PF_OK) return rc;
+  if (block != kTile) return fail(PF_EUNSUPPORTED, "block %d (supported: %d)", block, kTile);
+  if ((rc = pf_sparse_query_sizes(sh, start_pos, block, z)) != PF_OK) return rc;
+  if (z->nblk > 2048) return fail(PF_EUNSUPPORTED, "%lld key blocks (at most 2048)", z->nblk);
+  if (sh->Hkv * sh->d / 8 > 1024) return fail(PF_EUNSUPPORTED, "Hkv * d too large for pooling");
+  strides_or_default(sh->q_stride, sh->C, sh->Hq, sh->d, qs);
+  strides_or_default(sh->kh_stride, (long long)start_pos + sh->C, sh->Hkv, sh->d, ks);
+  if (!strides_ok(qs, 2) || !strides_ok(ks, 2))
+    return fail(PF_EINVAL, "q/k/v strides must be non-negative multiples of 16 bytes");
+  return PF_OK;
+}
+
+}  // namespace
+
+pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32_t start_pos,
+                         int32_t block, float alpha, const pf_sel* sel, void* stream) {
+  long long ks[3], qs[3];
+  pf_sparse_sizes z;
+  pf_status rc = check_sparse(sh, start_pos, block, ks, qs, &z);
+  if (rc != PF_OK) return rc;
+  if (!(alpha >= 0.f && alpha <= 1.f)) return fail(PF_EUNSUPPORTED, "alpha %g outside [0, 1]", alpha);
+  if (q == nullptr || k == nullptr || sel == nullptr || sel->row_bits == nullptr ||
+      sel->tile_list == nullptr || sel->tile_cnt == nullptr || sel->kbar == nullptr)
+    return fail(PF_EINVAL, "q, k and every pf_sel buffer must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(sel->kbar))
+    return fail(PF_EINVAL, "q, k and kbar must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = start_pos + sh->C;
+  PoolArgs p{};
+  p.x = k;
+  p.B = sh->B;
+  p.T = T;
+  p.H = sh->Hkv;
+  p.d = sh->d;
+  p.block = block;
+  p.nblk = (int)z.nblk;
+  p.sb = ks[0];
+  p.st = ks[1];
+  p.sh = ks[2];
+  p.out_f32 = sel->kbar;
+  p.out_lp = nullptr;
+  cudaError_t e = launch_pool(p, sh->in_dtype == PF_BF16 ? 1 : 0, st);
+  if (e != cudaSuccess) return cuda_fail(e, "pool launch");
+  IndexArgs ia{};
+  ia.q = q;
+  ia.ab_type = sh->in_dtype == PF_BF16 ? 1 : 0;
+  ia.B = sh->B;
+  ia.Hq = sh->Hq;
+  ia.Hkv = sh->Hkv;
+  ia.G = sh->Hq / sh->Hkv;
+  ia.d = sh->d;
+  ia.C = sh->C;
+  ia.s = start_pos;
+  ia.nblk = (int)z.nblk;
+  ia.n_qt = (int)z.nqt;
+  ia.words = (int)z.words;
+  ia.q_sb = qs[0];
+  ia.q_st = qs[1];
+  ia.q_sh = qs[2];
+  ia.kbar = sel->kbar;
+  ia.scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)sh->d);
+  ia.log_alpha = alpha > 0.f ? logf(alpha) : -INFINITY;
+  ia.row_bits = sel->row_bits;
+  ia.tile_list = sel->tile_list;
+  ia.tile_cnt = sel->tile_cnt;
+  if ((e = launch_index(ia, st)) != cudaSuccess) return cuda_fail(e, "index launch");
+  return PF_OK;
+}
+
+pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const void* v,
+                         int32_t start_pos, int32_t block, const pf_sel* sel, void* pooled,
+                         void* out, void* stream) {
+  long long ks[3], qs[3], os[3];
+  pf_sparse_sizes z;
+  pf_status rc = check_sparse(sh, start_pos, block, ks, qs, &z);
+  if (rc != PF_OK) return rc;
+  if (q == nullptr || k == nullptr || v == nullptr || sel == nullptr || pooled == nullptr ||
+      out == nullptr || sel->row_bits == nullptr || sel->tile_list == nullptr ||
+      sel->tile_cnt == nullptr || sel->kbar == nullptr)
+    return fail(PF_EINVAL, "q, k, v, sel buffers, pooled and out must be non-NULL");
+  const void* ptrs[] = {q, k, v, pooled, out, sel->kbar};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(PF_EINVAL, "every base pointer must be 16-byte aligned");
+  strides_or_default(sh->o_stride, sh->C, sh->Hq, sh->d, os);
+  if (!strides_ok(os, esize(sh->out_dtype))) return fail(PF_EINVAL, "out strides must be multiples of 16 bytes");
+  const int B = sh->B, C = sh->C, Hq = sh->Hq, Hkv = sh->Hkv, d = sh->d, T = start_pos + C;
+  const int nblk = (int)z.nblk;
+  const long long f32b = (z.kbar_elems * 4 + 255) / 256 * 256;
+  const long long lpb = (z.kbar_elems * 2 + 255) / 256 * 256;
+  float* vbar = static_cast<float*>(pooled);
+  void* kbar_lp = static_cast<char*>(pooled) + f32b;
+  void* vbar_lp = static_cast<char*>(pooled) + f32b + lpb;
+  const int bf16 = sh->in_dtype == PF_BF16 ? 1 : 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  PoolArgs p{};
+  p.x = v;
+  p.B = B;
+  p.T = T;
+  p.H = Hkv;
+  p.d = d;
+  p.block = block;
+  p.nblk = nblk;
+  p.sb = ks[0];
+  p.st = ks[1];
+  p.sh = ks[2];
+  p.out_f32 = vbar;
+  p.out_lp = vbar_lp;
+  cudaError_t e = launch_pool(p, bf16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "pool launch");
+  if ((e = launch_f32_to_lp(sel->kbar, kbar_lp, z.kbar_elems, bf16, st)) != cudaSuccess)
+    return cuda_fail(e, "kbar conversion");
+
+  AttnArgs a{};
+  fill_attn_common(sh, start_pos, a);
+  a.n_hist_tiles = 1 << 30;  // every exact key tile comes from the one K/V cache map
+  a.out = out;
+  a.o_sb = os[0];
+  a.o_st = os[1];
+  a.o_sh = os[2];
+  a.row_bits = sel->row_bits;
+  a.tile_list = sel->tile_list;
+  a.tile_cnt = sel->tile_cnt;
+  a.words = (int)z.words;
+  a.nblk = nblk;
+  a.log2_nb = log2f((float)block);
+
+  AttnMaps maps;
+  const pf_dtype dt = sh->in_dtype;
+  const long long pst[3] = {(long long)Hkv * nblk * d, (long long)nblk * d, (long long)d};
+  if ((rc = map_tokens(&maps.q, q, dt, B, C, Hq, d, qs, "q")) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.kh, k, dt, B, T, Hkv, d, ks, "k")) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.vh, v, dt, B, T, Hkv, d, ks, "v")) != PF_OK) return rc;
+  // pooled [B, Hkv, nblk, d]: dims (d, nblk, Hkv, B), box 64 x 128 pooled rows
+  if ((rc = make_map(&maps.kbar, kbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+                     "kbar")) != PF_OK)
+    return rc;
+  if ((rc = make_map(&maps.vbar, vbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+                     "vbar")) != PF_OK)
+    return rc;
+  maps.kc = maps.kh;
+  maps.vc = maps.vh;
+  if (a.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
+  if ((e = launch_attn(maps, a, MODE_SPARSE, st)) != cudaSuccess) return cuda_fail(e, "attention launch");
+  return PF_OK;
+}
+
+}  // extern "C"

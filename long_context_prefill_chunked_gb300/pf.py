@@ -1,0 +1,263 @@
+"""Python binding of libpf (ctypes): argument marshalling only.
+
+Every computation runs in libpf's CUDA kernels; PyTorch provides device
+memory and the stream.  Functions mirror the C ABI in include/pf.h:
+
+    attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, ...)
+    block_index(q, k, start_pos, block=128, alpha=0.1, sel=None)
+    attn_sparse(q, k, v, start_pos, sel, block=128, pooled=None, out=None)
+
+Tensors are token-major with the head dim contiguous: q [B, C, Hq, d],
+k_hist/v_hist [B, start_pos, Hkv, d], k_chunk/v_chunk [B, C, Hkv, d],
+k/v of the sparse path [B, start_pos + C, Hkv, d].  A missing libpf.so is an
+error (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpf.so")
+
+PF_OK, PF_EINVAL, PF_EUNSUPPORTED, PF_ECUDA, PF_ETIMEOUT = range(5)
+PF_F16, PF_BF16, PF_F32 = range(3)
+STATUS_NAMES = {0: "PF_OK", 1: "PF_EINVAL", 2: "PF_EUNSUPPORTED", 3: "PF_ECUDA", 4: "PF_ETIMEOUT"}
+
+EXPORTS = ["pf_attn_dense", "pf_block_index", "pf_attn_sparse", "pf_sparse_query_sizes",
+           "pf_stream_status", "pf_set_wait_timeout", "pf_set_debug_withhold", "pf_launch_count",
+           "pf_last_error", "pf_version"]
+
+
+class PFError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+I64x3 = ctypes.c_int64 * 3
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("C", ctypes.c_int32), ("in_dtype", ctypes.c_int),
+                ("out_dtype", ctypes.c_int), ("mask_dtype", ctypes.c_int), ("scale", ctypes.c_float),
+                ("q_stride", I64x3), ("kh_stride", I64x3), ("kc_stride", I64x3),
+                ("o_stride", I64x3), ("okv_stride", I64x3), ("mask_ld", ctypes.c_int64)]
+
+
+class Sel(ctypes.Structure):
+    _fields_ = [("row_bits", ctypes.c_void_p), ("tile_list", ctypes.c_void_p),
+                ("tile_cnt", ctypes.c_void_p), ("kbar", ctypes.c_void_p)]
+
+
+class SparseSizes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("nblk", "nqt", "words", "row_bits_elems", "tile_list_elems",
+                                              "tile_cnt_elems", "kbar_elems", "pooled_bytes")]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libpf.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libpf.so not found at %s: run __graft_entry__.build() first" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    V, I32, I64, F, P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.POINTER
+    lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V]
+    lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(Sel), V]
+    lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V]
+    lib.pf_sparse_query_sizes.argtypes = [P(Shape), I32, I32, P(SparseSizes)]
+    lib.pf_stream_status.argtypes = [V]
+    lib.pf_set_wait_timeout.argtypes = [I64]
+    lib.pf_set_wait_timeout.restype = None
+    lib.pf_set_debug_withhold.argtypes = [I32]
+    lib.pf_set_debug_withhold.restype = None
+    lib.pf_launch_count.argtypes = [I32]
+    lib.pf_launch_count.restype = I64
+    lib.pf_last_error.restype = ctypes.c_char_p
+    lib.pf_version.restype = ctypes.c_char_p
+    for name in ("pf_attn_dense", "pf_block_index", "pf_attn_sparse", "pf_sparse_query_sizes",
+                 "pf_stream_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != PF_OK:
+        raise PFError(rc, load().pf_last_error().decode())
+
+
+_DT = {torch.float16: PF_F16, torch.bfloat16: PF_BF16, torch.float32: PF_F32}
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    return _DT[t.dtype]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _bth(t: torch.Tensor):
+    """(b, t, h) element strides of a [B, T, H, d] tensor with d contiguous."""
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("expected a [B, T, H, d] tensor with a contiguous last dim")
+    return I64x3(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_shape(q, k_like, out_dtype, scale=0.0) -> Shape:
+    B, C, Hq, d = q.shape
+    sh = Shape()
+    sh.B, sh.Hq, sh.Hkv, sh.d, sh.C = B, Hq, k_like.shape[2], d, C
+    sh.in_dtype = _dtype(q)
+    sh.out_dtype = _DT[out_dtype]
+    sh.mask_dtype = PF_F32
+    sh.scale = float(scale)
+    sh.q_stride = _bth(q)
+    return sh
+
+
+def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=None, out_k=None,
+               out_v=None, out_dtype=torch.float32, scale=0.0, stream=None):
+    """Dense chunked prefill (pf_attn_dense); returns out [B, C, Hq, d]."""
+    lib = load()
+    B, C, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, C, Hq, d), dtype=out_dtype, device=q.device)
+    sh = make_shape(q, k_chunk, out.dtype, scale)
+    sh.kc_stride = _bth(k_chunk)
+    if v_chunk.stride() != k_chunk.stride():
+        raise ValueError("k_chunk and v_chunk must share strides")
+    if start_pos > 0:
+        sh.kh_stride = _bth(k_hist)
+        if v_hist.stride() != k_hist.stride():
+            raise ValueError("k_hist and v_hist must share strides")
+    sh.o_stride = _bth(out)
+    if out_k is not None:
+        if out_k.stride() != out_v.stride() or out_k.stride(3) != 1:
+            raise ValueError("out_k / out_v must share strides with a contiguous last dim")
+        sh.okv_stride = I64x3(out_k.stride(0), out_k.stride(1), out_k.stride(2))  # (b, h, t)
+    if mask is not None:
+        if mask.dim() != 2 or mask.stride(1) != 1:
+            raise ValueError("mask must be [C, start_pos + C] with contiguous rows")
+        sh.mask_dtype = _dtype(mask)
+        sh.mask_ld = mask.stride(0)
+    _check(lib.pf_attn_dense(ctypes.byref(sh), _ptr(q), _ptr(k_hist if start_pos > 0 else None),
+                             _ptr(v_hist if start_pos > 0 else None), _ptr(k_chunk), _ptr(v_chunk),
+                             _ptr(mask), int(start_pos), _ptr(out), _ptr(out_k), _ptr(out_v),
+                             _stream(stream)))
+    return out
+
+
+def sparse_sizes(q, k, start_pos, block=128) -> SparseSizes:
+    lib = load()
+    sh = make_shape(q, k, torch.float32)
+    z = SparseSizes()
+    _check(lib.pf_sparse_query_sizes(ctypes.byref(sh), int(start_pos), int(block), ctypes.byref(z)))
+    return z
+
+
+@dataclasses.dataclass
+class Selection:
+    """Device buffers of a pf_sel: row_bits [B,Hq,C,W] int32 (bit pattern), tile_list
+    [B,Hq,nqt,nblk], tile_cnt [B,Hq,nqt], kbar [B,Hkv,nblk,d] fp32."""
+    row_bits: torch.Tensor
+    tile_list: torch.Tensor
+    tile_cnt: torch.Tensor
+    kbar: torch.Tensor
+
+    def c_struct(self) -> Sel:
+        return Sel(self.row_bits.data_ptr(), self.tile_list.data_ptr(), self.tile_cnt.data_ptr(),
+                   self.kbar.data_ptr())
+
+
+def alloc_selection(q, k, start_pos, block=128) -> Selection:
+    z = sparse_sizes(q, k, start_pos, block)
+    B, C, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dev = q.device
+    return Selection(torch.empty((B, Hq, C, z.words), dtype=torch.int32, device=dev),
+                     torch.empty((B, Hq, z.nqt, z.nblk), dtype=torch.int32, device=dev),
+                     torch.empty((B, Hq, z.nqt), dtype=torch.int32, device=dev),
+                     torch.empty((B, Hkv, z.nblk, d), dtype=torch.float32, device=dev))
+
+
+def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stream=None) -> Selection:
+    """Pooled block selection (pf_block_index)."""
+    lib = load()
+    if sel is None:
+        sel = alloc_selection(q, k, start_pos, block)
+    sh = make_shape(q, k, torch.float32, scale)
+    sh.kh_stride = _bth(k)
+    cs = sel.c_struct()
+    _check(lib.pf_block_index(ctypes.byref(sh), _ptr(q), _ptr(k), int(start_pos), int(block),
+                              float(alpha), ctypes.byref(cs), _stream(stream)))
+    return sel
+
+
+def alloc_pooled(q, k, start_pos, block=128) -> torch.Tensor:
+    z = sparse_sizes(q, k, start_pos, block)
+    return torch.empty((z.pooled_bytes,), dtype=torch.uint8, device=q.device)
+
+
+def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=None,
+                out_dtype=torch.float32, scale=0.0, stream=None):
+    """Block-sparse attention with pooled correction (pf_attn_sparse); returns out."""
+    lib = load()
+    B, C, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, C, Hq, d), dtype=out_dtype, device=q.device)
+    if pooled is None:
+        pooled = alloc_pooled(q, k, start_pos, block)
+    if v.stride() != k.stride():
+        raise ValueError("k and v must share strides")
+    sh = make_shape(q, k, out.dtype, scale)
+    sh.kh_stride = _bth(k)
+    sh.o_stride = _bth(out)
+    cs = sel.c_struct()
+    _check(lib.pf_attn_sparse(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), int(start_pos), int(block),
+                              ctypes.byref(cs), _ptr(pooled), _ptr(out), _stream(stream)))
+    return out
+
+
+def vbar_view(pooled: torch.Tensor, q, k, start_pos, block=128) -> torch.Tensor:
+    """The fp32 block means of v at the head of the sparse workspace, [B, Hkv, nblk, d]."""
+    z = sparse_sizes(q, k, start_pos, block)
+    B, Hkv, d = q.shape[0], k.shape[2], q.shape[3]
+    return pooled[: z.kbar_elems * 4].view(torch.float32).view(B, Hkv, z.nblk, d)
+
+
+def stream_status(stream=None):
+    _check(load().pf_stream_status(_stream(stream)))
+
+
+def set_wait_timeout(cycles: int):
+    load().pf_set_wait_timeout(int(cycles))
+
+
+def set_debug_withhold(on: bool):
+    load().pf_set_debug_withhold(1 if on else 0)
+
+
+def launch_count(reset: bool = False) -> int:
+    return int(load().pf_launch_count(1 if reset else 0))
+
+
+def version() -> str:
+    return load().pf_version().decode()

@@ -1,0 +1,110 @@
+"""The C ABI without a GPU: the library loads, exports what include/pf.h declares,
+and refuses bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import long_context_prefill_chunked_gb300 as pfx
+from long_context_prefill_chunked_gb300 import pf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pf.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return pfx.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:pf_status|void|int64_t|const char\*)\s+(pf_\w+)\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "pf_attn_dense" in names and "pf_block_index" in names and "pf_attn_sparse" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pf.EXPORTS) <= set(names)
+
+
+def test_version(lib):
+    assert "sm_103a" in pfx.version()
+
+
+def shape(**kw):
+    sh = pf.Shape()
+    sh.B, sh.Hq, sh.Hkv, sh.d, sh.C = 1, 4, 2, 128, 256
+    sh.in_dtype, sh.out_dtype, sh.mask_dtype = pf.PF_BF16, pf.PF_F32, pf.PF_F32
+    for k, v in kw.items():
+        setattr(sh, k, v)
+    return sh
+
+
+FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x100008)
+
+
+def dense(lib, sh, q=FAKE, kh=None, vh=None, kc=FAKE, vc=FAKE, mask=None, s=0, out=FAKE, ok=None, ov=None):
+    return lib.pf_attn_dense(ctypes.byref(sh) if sh is not None else None, q, kh, vh, kc, vc, mask, s,
+                             out, ok, ov, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), pf.PF_EUNSUPPORTED),
+    (dict(Hq=6, Hkv=4), pf.PF_EINVAL),
+    (dict(C=0), pf.PF_EINVAL),
+    (dict(in_dtype=pf.PF_F32), pf.PF_EUNSUPPORTED),
+    (dict(scale=-1.0), pf.PF_EINVAL),
+])
+def test_dense_rejects_bad_shapes(lib, kw, code):
+    assert dense(lib, shape(**kw)) == code
+    assert lib.pf_last_error()
+
+
+def test_dense_rejects_bad_arguments(lib):
+    assert dense(lib, None) == pf.PF_EINVAL
+    assert dense(lib, shape(), q=None) == pf.PF_EINVAL
+    assert dense(lib, shape(), s=100, kh=FAKE, vh=FAKE) == pf.PF_EUNSUPPORTED   # start_pos % 128
+    assert dense(lib, shape(), s=128) == pf.PF_EINVAL                           # history missing
+    assert dense(lib, shape(), s=-128) == pf.PF_EINVAL
+    assert dense(lib, shape(), q=MISALIGNED) == pf.PF_EINVAL
+    assert dense(lib, shape(), ok=FAKE) == pf.PF_EINVAL                         # out_v missing
+    assert dense(lib, shape(mask_dtype=pf.PF_BF16), mask=FAKE) == pf.PF_EUNSUPPORTED
+    bad = shape()
+    bad.q_stride = pf.I64x3(256 * 4 * 128, 4 * 128, 60)                          # 120-byte head stride
+    assert dense(lib, bad) == pf.PF_EINVAL
+
+
+def test_sparse_rejects_bad_arguments(lib):
+    sel = pf.Sel(0x100000, 0x100000, 0x100000, 0x100000)
+    sh = shape()
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 64, 0.1, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, 1.5, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, -0.1, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
+    assert lib.pf_block_index(ctypes.byref(sh), None, FAKE, 0, 128, 0.1, ctypes.byref(sel), None) == pf.PF_EINVAL
+    assert lib.pf_attn_sparse(ctypes.byref(sh), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), None, FAKE, None) == pf.PF_EINVAL
+    long = shape(C=300000)
+    assert lib.pf_attn_sparse(ctypes.byref(long), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), FAKE, FAKE, None) == pf.PF_EUNSUPPORTED
+
+
+def test_sparse_sizes(lib):
+    sh = shape(C=4096, Hq=32, Hkv=8)
+    z = pf.SparseSizes()
+    assert lib.pf_sparse_query_sizes(ctypes.byref(sh), 8192, 128, ctypes.byref(z)) == pf.PF_OK
+    assert (z.nblk, z.nqt, z.words) == (96, 32, 3)
+    assert z.row_bits_elems == 32 * 4096 * 3
+    assert z.tile_list_elems == 32 * 32 * 96
+    assert z.kbar_elems == 8 * 96 * 128
+    assert z.pooled_bytes >= z.kbar_elems * (4 + 2 + 2)
+
+
+def test_header_cites_the_pages():
+    text = open(HEADER).read()
+    for page in ("ANE Prefill Research", "Porting FlashPrefill V2 to Apple silicon"):
+        assert page in text

@@ -1,0 +1,154 @@
+"""Dense chunked prefill: the CUDA path (through the C ABI) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import prefill_inputs as pi
+from gpu_util import assert_close, dev, errors, sample_rows, MAX_ABS
+
+pytestmark = pytest.mark.gpu
+
+pfx = pytest.importorskip("long_context_prefill_chunked_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    pfx.set_wait_timeout(400_000_000)
+    yield
+    pfx.stream_status()
+
+
+def run_chunk(w, s, mask=None, out_kv=False, out_dtype=torch.float32):
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(s))
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    ok = ov = None
+    if out_kv:
+        B, C, Hkv, d = kc.shape
+        ok = torch.empty((B, Hkv, C, d), dtype=kc.dtype, device="cuda")
+        ov = torch.empty_like(ok)
+    out = pfx.attn_dense(q, kh, vh, kc, vc, s, mask=dmask, out_k=ok, out_v=ov, out_dtype=out_dtype)
+    pfx.stream_status()
+    return out, ok, ov
+
+
+def ref_chunk(w, s, mask=None, rows=None, heads=None):
+    q, kh, vh, kc, vc = (w.f64(x) for x in w.chunk_views(s))
+    return oracle.dense(q, kh, vh, kc, vc, s, mask=None if mask is None else mask.astype(np.float64),
+                        rows=rows, heads=heads)
+
+
+# --------------------------------------------------------------------------- config 1
+@pytest.mark.parametrize("explicit", [True, False])
+def test_config1_tiny_dense(explicit):
+    w = pi.config(1)
+    mask = pi.causal_mask(w.chunk, 0) if explicit else None
+    out, _, _ = run_chunk(w, 0, mask)
+    assert_close(out, ref_chunk(w, 0, mask), "config 1")
+
+
+# --------------------------------------------------------------------------- config 2
+@pytest.fixture(scope="module")
+def cfg2():
+    return pi.config(2)
+
+
+@pytest.mark.parametrize("s", [0, 4096, 8192])
+def test_config2_gqa_chunked_every_row(cfg2, s):
+    """16q/8kv, d128, bf16, chunk 4096 at start 0/4096/8192 with the explicit causal mask."""
+    w = cfg2
+    mask = pi.causal_mask(w.chunk, s)
+    out, ok, ov = run_chunk(w, s, mask, out_kv=True)
+    assert_close(out, ref_chunk(w, s, mask), "config 2 s=%d" % s)
+    _, _, _, kc, vc = w.chunk_views(s)
+    assert np.array_equal(ok.cpu().view(torch.int16).numpy().view(np.uint16),
+                          np.transpose(kc, (0, 2, 1, 3)))
+    assert np.array_equal(ov.cpu().view(torch.int16).numpy().view(np.uint16),
+                          np.transpose(vc, (0, 2, 1, 3)))
+
+
+def test_config2_causal_default_matches_explicit_mask(cfg2):
+    out_m, _, _ = run_chunk(cfg2, 4096, pi.causal_mask(cfg2.chunk, 4096))
+    out_c, _, _ = run_chunk(cfg2, 4096, None)
+    mx, _ = errors(out_c, out_m.double().cpu().numpy())
+    assert mx <= 1e-3
+
+
+# --------------------------------------------------------------------------- config 3
+def test_config3_folded_indexer_mask():
+    """Arbitrary mask: 512 compressed blocks of 4 per query over an 8192-token history."""
+    w = pi.config(3)
+    s = 8192
+    mask, _ = pi.indexer_fold_mask(w.seed, w.chunk, s)
+    out, _, _ = run_chunk(w, s, mask)
+    ref = ref_chunk(w, s, mask)
+    assert_close(out, ref, "config 3")
+    # negative control: the causal-only arm must land >= 10x the tolerance away
+    causal, _, _ = run_chunk(w, s, None)
+    mx, _ = errors(causal, ref)
+    assert mx >= 10 * MAX_ABS, mx
+
+
+def test_config3_fp16_mask_matches():
+    w = pi.config(3)
+    s = 8192
+    mask, _ = pi.indexer_fold_mask(w.seed, w.chunk, s)
+    rows = sample_rows(w.chunk, 256, 3)
+    out, _, _ = run_chunk(w, s, mask.astype(np.float16))
+    assert_close(out[:, rows], ref_chunk(w, s, mask, rows=rows), "config 3 fp16 mask")
+
+
+# --------------------------------------------------------------------------- edges
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 128), ("bf16", 64), ("f16", 64)])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (6, 2), (3, 3)])
+def test_ragged_chunks(dtype, d, Hq, Hkv):
+    """Ragged chunk (C = 200, not a multiple of 128) over a 256-row history; GQA 2, 3 and 1."""
+    w = pi.normal_workload("ragged", 11, 2, Hq, Hkv, d, 456, 200, dtype)
+    for s in (0, 256):
+        out, _, _ = run_chunk(w, s)
+        assert_close(out, ref_chunk(w, s), "ragged s=%d" % s)
+
+
+def test_ragged_explicit_mask_random_values():
+    w = pi.normal_workload("ragged-mask", 12, 1, 4, 2, 128, 457, 201, "bf16")
+    s = 256
+    g = np.random.default_rng(5)
+    mask = g.uniform(-4.0, 0.0, size=(w.chunk, s + w.chunk)).astype(np.float32)
+    mask[g.random(mask.shape) < 0.5] = -30000.0
+    mask[7, :] = -30000.0          # a fully masked row: plain softmax over the raw scores
+    out, _, _ = run_chunk(w, s, mask)
+    assert_close(out, ref_chunk(w, s, mask), "random mask")
+
+
+def test_bf16_output_and_strided_query():
+    w = pi.normal_workload("strided", 13, 1, 8, 4, 128, 640, 384, "bf16")
+    s = 256
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(s))
+    big = torch.zeros((1, 384, 12, 128), dtype=q.dtype, device="cuda")
+    big[:, :, 2:10] = q
+    qv = big[:, :, 2:10]                               # non-contiguous head slice
+    out = pfx.attn_dense(qv, kh, vh, kc, vc, s, out_dtype=torch.bfloat16)
+    pfx.stream_status()
+    ref = ref_chunk(w, s)
+    mx, _ = errors(out, ref)
+    assert mx <= 5e-3 + 2 ** -8 * np.abs(ref).max()      # bf16 output adds half an ulp
+
+
+def test_chunked_equals_one_shot_on_gpu():
+    w = pi.normal_workload("oneshot", 14, 1, 8, 2, 128, 1024, 256, "bf16")
+    q, k, v = dev(w.q, "bf16"), dev(w.k, "bf16"), dev(w.v, "bf16")
+    one = pfx.attn_dense(q, k[:, :0], v[:, :0], k, v, 0)
+    for s in range(0, 1024, 256):
+        part = pfx.attn_dense(q[:, s:s + 256], k[:, :s], v[:, :s], k[:, s:s + 256], v[:, s:s + 256], s)
+        mx, _ = errors(part, one[:, s:s + 256].double().cpu().numpy())
+        assert mx <= 2e-3
+    pfx.stream_status()
+
+
+def test_launch_counter_counts_kernels():
+    w = pi.config(1)
+    pfx.launch_count(reset=True)
+    run_chunk(w, 0, None, out_kv=True)
+    assert pfx.launch_count() == 3      # attention + two cache-layout copies
