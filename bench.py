@@ -1,0 +1,370 @@
+"""Benchmark: long-context prefill attention at 32K tokens on GB300.
+
+One step = one 32K-token prompt (32 query heads, 8 KV heads, head_dim 128,
+bf16, planted block structure) through the whole path:
+  * dense chunked prefill: 8 chunks of 4096 rows, each causal over the
+    previous chunks' K/V, emitting the chunk's K/V into a head-major cache;
+  * block-sparse prefill of the same prompt: block index (pool, score,
+    select, compact) + exact kept blocks with the pooled correction.
+The metric is dense-equivalent TFLOP/s: 4 * Hq * d * (causal query-key pairs)
+per path, summed, over the step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica (weak scaling);
+time is the max over ranks.  ``--impl reference`` times the float64 CPU oracle
+instead (bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attention TFLOP/s (dense-equiv) & tokens/s at 32K; % of bf16 TC peak"
+N_TOK, HQ, HKV, D, CHUNK, BLOCK, ALPHA = 32768, 32, 8, 128, 4096, 128, 0.1
+WORKLOAD = ("32K-token prompt, 32q/8kv heads, d128, bf16, planted blocks (beta %g); dense chunked "
+            "prefill 8x4096 causal + block-sparse prefill (block 128, alpha 0.1)")
+
+
+def pairs_causal(C, s):
+    return C * s + C * (C + 1) // 2
+
+
+def flops_equiv(C, s, Hq=HQ, d=D):
+    return 4.0 * Hq * d * pairs_causal(C, s)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return j, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.gpu = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------- oracle legs
+def oracle_sample_rate(w, seconds, seed=0):
+    """Time the float64 oracle on sampled rows of both paths; returns (TFLOP/s equiv, detail)."""
+    import oracle
+    g = np.random.default_rng(seed)
+    s_last = N_TOK - CHUNK
+    q_last = w.f64(w.q[:, s_last:])
+    kh, vh = w.f64(w.k[:, :s_last]), w.f64(w.v[:, :s_last])
+    kc, vc = w.f64(w.k[:, s_last:]), w.f64(w.v[:, s_last:])
+    q_all, k_all, v_all = w.f64(w.q), w.f64(w.k), w.f64(w.v)
+    flops = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        rows = np.sort(g.choice(CHUNK, size=16, replace=False))
+        oracle.dense(q_last, kh, vh, kc, vc, s_last, rows=rows)
+        flops += sum(4.0 * HQ * D * (s_last + r + 1) for r in rows)
+        srows = np.sort(g.choice(N_TOK, size=16, replace=False))
+        oracle.sparse(q_all, k_all, v_all, 0, BLOCK, ALPHA, rows=srows)
+        flops += sum(4.0 * HQ * D * (r + 1) for r in srows)
+        rows_done += 32
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, {"rows": rows_done, "seconds": dt, "threads": _blas_threads()}
+
+
+def _blas_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max((i.get("num_threads", 1) for i in info), default=os.cpu_count())
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import prefill_inputs as pi
+    w = pi.config(4)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        v, det = oracle_sample_rate(w, 2.0, seed=i)
+        if i >= args.warmup:
+            per_step.append((v, det))
+    value = statistics.mean(v for v, _ in per_step)
+    rows = sum(d["rows"] for _, d in per_step)
+    secs = sum(d["seconds"] for _, d in per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": WORKLOAD % pi.PLANT_BETA},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": per_step[0][1]["threads"],
+                         "kind": "oracle",
+                         "sample": "%d query rows x 32 heads (half from the last dense chunk, half "
+                                   "block-sparse), float64 numpy oracle" % rows},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- ours
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import long_context_prefill_chunked_gb300 as pfx
+    import prefill_inputs as pi
+
+    w = pi.config(4)
+    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    Q, K, V = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    out_d = torch.empty((1, N_TOK, HQ, D), dtype=torch.float32, device=dev)
+    out_s = torch.empty_like(out_d)
+    cache_k = torch.empty((1, HKV, N_TOK, D), dtype=torch.bfloat16, device=dev)
+    cache_v = torch.empty_like(cache_k)
+    sel = pfx.alloc_selection(Q, K, 0, BLOCK)
+    pooled = pfx.alloc_pooled(Q, K, 0, BLOCK)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    starts = list(range(0, N_TOK, CHUNK))
+
+    def mk():
+        return torch.cuda.Event(enable_timing=True)
+
+    def step(q, k, v, ev=None):
+        for i, s in enumerate(starts):
+            if ev is not None:
+                ev["dense"][i][0].record(stream)
+            pfx.attn_dense(q[:, s:s + CHUNK], k[:, :s], v[:, :s], k[:, s:s + CHUNK], v[:, s:s + CHUNK], s,
+                           out=out_d[:, s:s + CHUNK], out_k=cache_k[:, :, s:s + CHUNK],
+                           out_v=cache_v[:, :, s:s + CHUNK], stream=stream)
+            if ev is not None:
+                ev["dense"][i][1].record(stream)
+        if ev is not None:
+            ev["index"][0].record(stream)
+        pfx.block_index(q, k, 0, BLOCK, ALPHA, sel=sel, stream=stream)
+        if ev is not None:
+            ev["index"][1].record(stream)
+            ev["sparse"][0].record(stream)
+        pfx.attn_sparse(q, k, v, 0, sel, block=BLOCK, pooled=pooled, out=out_s, stream=stream)
+        if ev is not None:
+            ev["sparse"][1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(Q, K, V)
+    pfx.stream_status(stream)
+
+    evs = [{"dense": [(mk(), mk()) for _ in starts], "index": (mk(), mk()), "sparse": (mk(), mk()),
+            "step": (mk(), mk())} for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    pfx.launch_count(reset=True)
+    for i in range(args.steps):
+        flush.zero_()                       # L2 flush between steps (outside the step window)
+        evs[i]["step"][0].record(stream)
+        step(Q, K, V, evs[i])
+        evs[i]["step"][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = pfx.launch_count()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    pfx.stream_status(stream)
+
+    step_ms = [e["step"][0].elapsed_time(e["step"][1]) for e in evs]
+    dense_ms = [[a.elapsed_time(b) for a, b in e["dense"]] for e in evs]
+    index_ms = [e["index"][0].elapsed_time(e["index"][1]) for e in evs]
+    sparse_ms = [e["sparse"][0].elapsed_time(e["sparse"][1]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+
+    f_dense = sum(flops_equiv(CHUNK, s) for s in starts)
+    f_sparse = flops_equiv(N_TOK, 0)
+    value = world * (f_dense + f_sparse) / (ms_step * 1e-3) / 1e12
+    tokens_per_s = world * 2 * N_TOK / (ms_step * 1e-3)
+
+    # dominant kernel: the dense attention launches (8 per step)
+    d_ms = sum(map(sum, dense_ms)) / args.steps
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = f_dense / (d_ms * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "attn_dense_traffic.json")
+    if os.path.exists(tpath):
+        traffic = json.load(open(tpath)).get("bytes_per_launch")
+
+    tc = sel.tile_cnt.cpu().numpy().astype(np.float64)
+    n_qt = tc.shape[-1]
+    cand = HQ * sum(range(n_qt))
+    skip_tiles = 1.0 - (tc - 1).sum() / cand
+
+    # e2e: host buffers in, host buffers out, through the same public API
+    hq = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(w.k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(w.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ho_d = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    ho_s = torch.empty(out_s.shape, dtype=out_s.dtype).pin_memory()
+    hck = torch.empty(cache_k.shape, dtype=cache_k.dtype).pin_memory()
+    hcv = torch.empty(cache_v.shape, dtype=cache_v.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    e0, e1 = mk(), mk()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        step(dq, dk, dv)
+        ho_d.copy_(out_d, non_blocking=True)
+        ho_s.copy_(out_s, non_blocking=True)
+        hck.copy_(cache_k, non_blocking=True)
+        hcv.copy_(cache_v, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    pfx.stream_status(stream)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = sum(x.numel() * x.element_size() for x in (ho_d, ho_s, hck, hcv))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) Q/K/V with planted key blocks (no dataset)",
+        "config": {"workload": WORKLOAD % w.beta, "tokens": N_TOK, "Hq": HQ, "Hkv": HKV, "head_dim": D,
+                   "chunk": CHUNK, "block": BLOCK, "alpha": ALPHA, "out_dtype": "f32",
+                   "l2": "flushed between steps (256 MB write outside the step window)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": tokens_per_s,
+        "paths": {
+            "dense_chunked": {"ms": sum(map(sum, dense_ms)) / args.steps,
+                              "tflops_equiv": f_dense / (d_ms * 1e-3) / 1e12,
+                              "tokens_per_s": N_TOK / (d_ms * 1e-3),
+                              "ms_per_chunk": [statistics.mean(x[i] for x in dense_ms) for i in range(len(starts))]},
+            "block_sparse": {"ms": statistics.mean(index_ms) + statistics.mean(sparse_ms),
+                             "index_ms": statistics.mean(index_ms), "attn_ms": statistics.mean(sparse_ms),
+                             "tflops_equiv": f_sparse / ((statistics.mean(index_ms) + statistics.mean(sparse_ms)) * 1e-3) / 1e12,
+                             "skip_share_tiles": skip_tiles},
+        },
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<causal> (8 launches per step; window includes the "
+                               "chunk's two cache-layout copies)",
+                     "peak_source": "%s bf16_tflops (burst)" % peak_src},
+        "e2e": {"value": world * (f_dense + f_sparse) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, det = oracle_sample_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": det["threads"], "kind": "oracle",
+                                "sample": "%d query rows x 32 heads in %.1f s: half from the last dense "
+                                          "chunk (keys 28672..32767), half block-sparse; float64 numpy "
+                                          "oracle" % (det["rows"], det["seconds"])}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
