@@ -170,6 +170,49 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------------------------- profiling cases
+def run_case(args):
+    """Small cases for ncu: the last dense chunk of the 32K prompt (K/V 134 MB, larger than L2)
+    or the 32K block-sparse pair.  Prints per-iteration times; not a bench line."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import long_context_prefill_chunked_gb300 as pfx
+    import prefill_inputs as pi
+    w = pi.config(4)
+    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    s = N_TOK - CHUNK
+    K, V = to_dev(w.k), to_dev(w.v)
+    Q = to_dev(w.q[:, s:]) if args.case == "dense-chunk" else to_dev(w.q)
+    if args.case == "dense-chunk":
+        out = torch.empty((1, CHUNK, HQ, D), dtype=torch.float32, device="cuda")
+        run = lambda: pfx.attn_dense(Q, K[:, :s], V[:, :s], K[:, s:], V[:, s:], s, out=out)
+        flops = flops_equiv(CHUNK, s)
+    else:
+        sel = pfx.alloc_selection(Q, K, 0)
+        pooled = pfx.alloc_pooled(Q, K, 0)
+        out = torch.empty((1, N_TOK, HQ, D), dtype=torch.float32, device="cuda")
+
+        def run():
+            pfx.block_index(Q, K, 0, BLOCK, ALPHA, sel=sel)
+            pfx.attn_sparse(Q, K, V, 0, sel, pooled=pooled, out=out)
+        flops = flops_equiv(N_TOK, 0)
+    for _ in range(args.warmup):
+        run()
+    pfx.stream_status()
+    times = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    pfx.stream_status()
+    print(json.dumps({"case": args.case, "ms": times, "tflops_equiv": flops / (min(times) * 1e-3) / 1e12}))
+    return 0
+
+
 # ---------------------------------------------------------------------------- ours
 def main():
     ap = argparse.ArgumentParser()
@@ -180,9 +223,14 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse"],
+                    help="dense-chunk / sparse: a small profiling case (one 4096-row chunk at "
+                         "start 28672, or the 32K block-sparse pair), timings only")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.case != "full":
+        return run_case(args)
 
     import torch
     import torch.distributed as dist

@@ -61,7 +61,8 @@ typedef enum {
   PF_EINVAL = 1,
   PF_EUNSUPPORTED = 2,
   PF_ECUDA = 3,
-  PF_ETIMEOUT = 4
+  PF_ETIMEOUT = 4,
+  PF_ERANGE = 5
 } pf_status;
 
 typedef enum { PF_F16 = 0, PF_BF16 = 1, PF_F32 = 2 } pf_dtype;
@@ -154,8 +155,9 @@ pf_status pf_attn_sparse(const pf_shape* shape, const void* q, const void* k, co
                          void* out, void* stream);
 
 /* Synchronise `stream`, then report (and clear) a device-side error: PF_ETIMEOUT
- * if a bounded wait in a kernel gave up since the last check, PF_ECUDA on a CUDA
- * error, else PF_OK. */
+ * if a bounded wait in a kernel gave up since the last check; PF_ERANGE if a
+ * bf16 v held a value the fp16 P*V product cannot represent (|v| > 65504, inf or
+ * nan: the output is then invalid); PF_ECUDA on a CUDA error; else PF_OK. */
 pf_status pf_stream_status(void* stream);
 
 /* Bounded-wait limit in SM clock cycles (default 4e8, about 0.2 s). */

@@ -14,15 +14,20 @@
 // load feeds both heads' MMAs.
 //   warps 0-3  softmax for slot 0 (thread t owns query row t = TMEM lane t)
 //   warps 4-7  softmax for slot 1
-//   warp  8    TMA producer (Q once, then K/V tiles through a 2-stage ring)
+//   warp  8    TMA producer (Q once, then K and V tiles through two 2-stage rings)
 //   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
-//   warps 10-11 spare (they complete the third warpgroup for setmaxnreg)
+//   warps 10-11 V converters: for bf16 inputs they rewrite each landed V tile
+//              in place as fp16, so that P * V runs as an fp16 MMA (P carries
+//              11 significant bits instead of bf16's 8; bf16 -> fp16 is exact
+//              for |v| <= 65504 and larger values are reported as an error)
 // Tensor memory (512 columns): slot s uses columns [256s, 256s+128) for S (P
-// is written back over its first half as 16-bit pairs) and [256s+128,
+// is written back over its first half as fp16 pairs) and [256s+128,
 // 256s+128+d) for the fp32 O accumulator.
 // MMA order per key tile j: PV(slot0, j), S(slot0, j+1), PV(slot1, j),
 // S(slot1, j+1); each softmax group works on its tile while the tensor core
-// runs the other slot's pair.
+// runs the other slot's pair.  K and V have separate rings: a K stage is freed
+// as soon as both S MMAs that read it are done, so K tile j+1 is in flight
+// while tile j's softmax runs.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -47,8 +52,10 @@ enum {
   B_Q = 0,
   B_KF = 1,             // K tile landed, per stage
   B_VF = B_KF + NST,    // V tile landed, per stage
-  B_KE = B_VF + NST,    // stage free again (both slots' MMAs on it done)
-  B_SF = B_KE + NST,    // S ready, per slot
+  B_VC = B_VF + NST,    // V tile converted to fp16 (bf16 inputs), per stage
+  B_KE = B_VC + NST,    // K stage free again (both slots' S MMAs done)
+  B_VE = B_KE + NST,    // V stage free again (both slots' PV MMAs done)
+  B_SF = B_VE + NST,    // S ready, per slot
   B_PF = B_SF + 2,      // P written (and O rescaled), per slot
   B_OF = B_PF + 2,      // last PV done
   B_DR = B_OF + 1,      // drain: all issued MMAs done
@@ -62,7 +69,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
 // where-codes recorded with a timeout: (role << 8) | barrier
-enum { R_PROD = 1, R_MMA = 2, R_SOFT = 3 };
+enum { R_PROD = 1, R_MMA = 2, R_SOFT = 3, R_CONV = 4 };
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, long long timeout,
                                          volatile int* abort_flag, unsigned* status,
@@ -84,14 +91,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 }
 
 __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&x)[128]) {
-  uint32_t r[32];
+  uint32_t r[128];
+  tmem_ld128_wait(taddr, r);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    tmem_ld32(taddr + 32 * q, r);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[32 * q + i] = __uint_as_float(r[i]);
-  }
+  for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(r[i]);
 }
 
 template <int MODE>
@@ -124,7 +127,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int st = 0; st < NST; ++st) {
       mbar_init(BAR(B_KF + st), 1);
       mbar_init(BAR(B_VF + st), 1);
+      mbar_init(BAR(B_VC + st), 2);
       mbar_init(BAR(B_KE + st), 1);
+      mbar_init(BAR(B_VE + st), 1);
     }
     for (int sl = 0; sl < 2; ++sl) {
       mbar_init(BAR(B_SF + sl), 1);
@@ -195,10 +200,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     n_tiles = n_pool + *n_ex_slot;
   }
 
-  // 384 threads x 168 registers at launch; the softmax warpgroups take 232,
-  // the producer/MMA warpgroup keeps 40: 2*128*232 + 128*40 = 384*168.
+  // 384 threads x 168 registers at launch; the softmax warpgroups take 224,
+  // the producer/MMA/converter warpgroup keeps 56: 2*128*224 + 128*56 = 384*168.
   if (warp >= 8) {
-    regs_dec<40>();
+    regs_dec<72>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -214,11 +219,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < nd; ++c)
           tma_load_4d(sb + SM_Q + 32768u * sl + 16384u * c, &maps.q, BAR(B_Q), 64 * c, h0 + sl,
                       q0, b);
+      int last_k[NST], last_v[NST];
+      for (int st = 0; st < NST; ++st) last_k[st] = last_v[st] = -1;
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NST, use = j / NST;
-        if (use > 0 && !mbar_wait(BAR(B_KE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
-                                  (R_PROD << 8) | (B_KE + st)))
-          break;
         const CUtensorMap *mk, *mv;
         int c1, c2;
         if (MODE == MODE_SPARSE && j < n_pool) {
@@ -239,21 +243,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           c1 = g;
         }
+        if (use > 0 && !mbar_wait(BAR(B_KE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
+                                  (R_PROD << 8) | (B_KE + st)))
+          break;
         mbar_arrive_expect_tx(BAR(B_KF + st), tile_bytes);
         for (int c = 0; c < nd; ++c)
           tma_load_4d(sb + SM_K + 32768u * st + 16384u * c, mk, BAR(B_KF + st), 64 * c, c1, c2, b);
+        last_k[st] = use;
+        if (use > 0 && !mbar_wait(BAR(B_VE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
+                                  (R_PROD << 8) | (B_VE + st)))
+          break;
         mbar_arrive_expect_tx(BAR(B_VF + st), tile_bytes);
         for (int c = 0; c < nd; ++c)
           tma_load_4d(sb + SM_V + 32768u * st + 16384u * c, mv, BAR(B_VF + st), 64 * c, c1, c2, b);
-        last_use[st] = use;
+        last_v[st] = use;
       }
       if (*abort_flag) {  // let this warp's copies land before the CTA exits
         drain_wait(BAR(B_Q), 0, a.timeout, a.status);
-        for (int st = 0; st < NST; ++st)
-          if (last_use[st] >= 0) {
-            drain_wait(BAR(B_KF + st), last_use[st] & 1, a.timeout, a.status);
-            drain_wait(BAR(B_VF + st), last_use[st] & 1, a.timeout, a.status);
-          }
+        for (int st = 0; st < NST; ++st) {
+          if (last_k[st] >= 0) drain_wait(BAR(B_KF + st), last_k[st] & 1, a.timeout, a.status);
+          if (last_v[st] >= 0) drain_wait(BAR(B_VF + st), last_v[st] & 1, a.timeout, a.status);
+        }
       }
     }
     __syncwarp();
@@ -261,26 +271,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc_f16((uint32_t)a.ab_type, 128, 128, 0);
-      const uint32_t idesc_pv = make_idesc_f16((uint32_t)a.ab_type, 128, (uint32_t)a.d, 1);
+      const uint32_t idesc_pv = make_idesc_f16(0u, 128, (uint32_t)a.d, 1);  // fp16 P x fp16 V
       const int kq = a.d / 16;
+      // descriptors are built once; a k-step only advances the start-address field
+      const uint64_t dq0 = make_sdesc_sw128(sb + SM_Q, 16, 1024);
+      const uint64_t dk0 = make_sdesc_sw128(sb + SM_K, 16, 1024);
+      const uint64_t dv0 = make_sdesc_sw128(sb + SM_V, 16384, 1024);
       auto issue_qk = [&](int sl, int st) {
         const uint32_t d_tmem = tmem + 256u * sl;
-#pragma unroll 1
-        for (int kk = 0; kk < kq; ++kk) {
-          const uint32_t off = 16384u * (kk >> 2) + 32u * (kk & 3);
-          const uint64_t ad = make_sdesc_sw128(sb + SM_Q + 32768u * sl + off, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(sb + SM_K + 32768u * st + off, 16, 1024);
-          mma_ss(d_tmem, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        const uint64_t aq = dq0 + ((32768u * sl) >> 4);
+        const uint64_t bk = dk0 + ((32768u * st) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          if (kk < kq) {
+            const uint32_t off = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+            mma_ss(d_tmem, aq + off, bk + off, idesc_qk, kk > 0 ? 1u : 0u);
+          }
         }
       };
       auto issue_pv = [&](int sl, int st, bool acc) {
         const uint32_t d_tmem = tmem + 256u * sl + 128u;
-#pragma unroll 1
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bd = make_sdesc_sw128(sb + SM_V + 32768u * st + 2048u * kk, 16384, 1024);
-          mma_ts(d_tmem, tmem + 256u * sl + 8u * kk, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
+        const uint64_t bv = dv0 + ((32768u * st) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(d_tmem, tmem + 256u * sl + 8u * kk, bv + ((2048u * kk) >> 4), idesc_pv,
+                 (acc || kk > 0) ? 1u : 0u);
       };
+      const int vbar_first = a.convert_v ? B_VC : B_VF;
       bool ok = mbar_wait(BAR(B_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | B_Q);
       tc_fence_after();
       for (int j = 0; ok && j < n_tiles; ++j) {
@@ -294,10 +311,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             issue_qk(sl, st);
             if (!a.withhold) tc_commit(BAR(B_SF + sl));
           }
+          tc_commit(BAR(B_KE + st));
         }
-        ok = mbar_wait(BAR(B_VF + st), ph, a.timeout, abort_flag, a.status, (R_MMA << 8) | (B_VF + st));
+        ok = mbar_wait(BAR(vbar_first + st), ph, a.timeout, abort_flag, a.status,
+                       (R_MMA << 8) | (vbar_first + st));
         if (!ok) break;
         tc_fence_after();
+        const int st1 = (j + 1) % NST;
         for (int sl = 0; sl < a.slots; ++sl) {
           ok = mbar_wait(BAR(B_PF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
                          (R_MMA << 8) | (B_PF + sl));
@@ -305,7 +325,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc_fence_after();
           issue_pv(sl, st, j > 0);
           if (j + 1 < n_tiles) {
-            const int st1 = (j + 1) % NST;
             if (sl == 0) {
               ok = mbar_wait(BAR(B_KF + st1), (uint32_t)((j + 1) / NST) & 1u, a.timeout,
                              abort_flag, a.status, (R_MMA << 8) | (B_KF + st1));
@@ -317,16 +336,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(BAR(B_KE + st));
+        if (j + 1 < n_tiles) tc_commit(BAR(B_KE + st1));
+        tc_commit(BAR(B_VE + st));
       }
       if (ok) tc_commit(BAR(B_OF));
       tc_commit(BAR(B_DR));  // no MMA may still run when tensor memory is released
       drain_wait(BAR(B_DR), 0, a.timeout, a.status);
     }
     __syncwarp();
+  } else if (warp >= 10 && a.convert_v) {
+    // ------------------------------------------------------------ V converters
+    const int ct = threadIdx.x - 320;  // 0..63
+    const int nvec = (a.d / 64) * 1024;  // 16-byte vectors per V tile
+    uint32_t bad = 0u;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % NST;
+      if (!wait_all(BAR(B_VF + st), (uint32_t)(j / NST) & 1u, a.timeout, abort_flag, a.status,
+                    (R_CONV << 8) | (B_VF + st)))
+        break;
+      uint4* v = reinterpret_cast<uint4*>(smem + SM_V + 32768u * st);
+      for (int i = ct; i < nvec; i += 64) {
+        uint4 w = v[i];
+        uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          bad |= __vcmpgeu2(ww[e] & 0x7FFF7FFFu, 0x47804780u);  // |v| > 65504, inf or nan
+          ww[e] = pack_f16(__uint_as_float(ww[e] << 16), __uint_as_float(ww[e] & 0xFFFF0000u));
+        }
+        v[i] = w;
+      }
+      fence_proxy_async();  // generic-proxy writes -> visible to the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_VC + st));
+    }
+    if (__any_sync(0xffffffffu, bad != 0u) && lane == 0) record_error(a.status, ST_VRANGE, R_CONV << 8);
   }
   } else {
-    regs_inc<232>();
+    regs_inc<216>();
   if ((warp >> 2) < a.slots) {
     // ------------------------------------------------------------ softmax
     const int sl = warp >> 2;
@@ -364,39 +410,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint4* mp = reinterpret_cast<const uint4*>(
                 reinterpret_cast<const __half*>(a.mask) + (long long)row * a.mask_ld + key0);
 #pragma unroll
-            for (int v = 0; v < 16; ++v) {
-              const uint4 w = __ldg(mp + v);
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            for (int q = 0; q < 4; ++q) {  // 32 columns at a time keeps the loads in registers
+              uint4 w4[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
-                x[8 * v + 2 * e] = fmaf(x[8 * v + 2 * e], a.scale_log2, f.x * kLog2e);
-                x[8 * v + 2 * e + 1] = fmaf(x[8 * v + 2 * e + 1], a.scale_log2, f.y * kLog2e);
+              for (int v = 0; v < 4; ++v) w4[v] = __ldg(mp + 4 * q + v);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint32_t ww[4] = {w4[v].x, w4[v].y, w4[v].z, w4[v].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+                  const int c = 32 * q + 8 * v + 2 * e;
+                  x[c] = fmaf(x[c], a.scale_log2, f.x * kLog2e);
+                  x[c + 1] = fmaf(x[c + 1], a.scale_log2, f.y * kLog2e);
+                }
               }
+              asm volatile("" ::: "memory");
             }
           } else {
             const float4* mp = reinterpret_cast<const float4*>(
                 reinterpret_cast<const float*>(a.mask) + (long long)row * a.mask_ld + key0);
 #pragma unroll
-            for (int v = 0; v < 32; ++v) {
-              const float4 w = __ldg(mp + v);
-              x[4 * v + 0] = fmaf(x[4 * v + 0], a.scale_log2, w.x * kLog2e);
-              x[4 * v + 1] = fmaf(x[4 * v + 1], a.scale_log2, w.y * kLog2e);
-              x[4 * v + 2] = fmaf(x[4 * v + 2], a.scale_log2, w.z * kLog2e);
-              x[4 * v + 3] = fmaf(x[4 * v + 3], a.scale_log2, w.w * kLog2e);
+            for (int q = 0; q < 4; ++q) {
+              float4 w4[8];
+#pragma unroll
+              for (int v = 0; v < 8; ++v) w4[v] = __ldg(mp + 8 * q + v);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const int c = 32 * q + 4 * v;
+                x[c + 0] = fmaf(x[c + 0], a.scale_log2, w4[v].x * kLog2e);
+                x[c + 1] = fmaf(x[c + 1], a.scale_log2, w4[v].y * kLog2e);
+                x[c + 2] = fmaf(x[c + 2], a.scale_log2, w4[v].z * kLog2e);
+                x[c + 3] = fmaf(x[c + 3], a.scale_log2, w4[v].w * kLog2e);
+              }
+              asm volatile("" ::: "memory");
             }
           }
-        } else {
+        } else {  // ragged last tile, unaligned rows or a padding row: element loads
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int key = key0 + c;
-            float mv = 0.f;
-            if (valid && key < a.T) {
-              const long long o = (long long)row * a.mask_ld + key;
-              mv = a.mask_f16 ? __half2float(reinterpret_cast<const __half*>(a.mask)[o])
-                              : reinterpret_cast<const float*>(a.mask)[o];
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int c = 32 * q + i;
+              const int key = key0 + c;
+              float mv = 0.f;
+              if (valid && key < a.T) {
+                const long long o = (long long)row * a.mask_ld + key;
+                mv = a.mask_f16 ? __half2float(reinterpret_cast<const __half*>(a.mask)[o])
+                                : reinterpret_cast<const float*>(a.mask)[o];
+              }
+              x[c] = (key < a.T) ? fmaf(x[c], a.scale_log2, mv * kLog2e) : -INFINITY;
             }
-            x[c] = (key < a.T) ? fmaf(x[c], a.scale_log2, mv * kLog2e) : -INFINITY;
+            asm volatile("" ::: "memory");
           }
         }
       } else {  // MODE_SPARSE
@@ -469,7 +534,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float p1 = ex2(fmaf(x[32 * q + 2 * i + 1], xs, off));
           ls0 += p0;
           ls1 += p1;
-          pk[i] = a.ab_type ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+          pk[i] = pack_f16(p0, p1);
         }
         tmem_st16(t_s + 16u * q, pk);
       }

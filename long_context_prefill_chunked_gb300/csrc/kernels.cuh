@@ -7,7 +7,7 @@
 namespace pf {
 
 constexpr int kTile = 128;        // query rows and keys per tile (= key block of the sparse path)
-constexpr int kAttnThreads = 384; // 8 softmax warps (2 slots x 4), TMA warp, MMA warp, 2 spare
+constexpr int kAttnThreads = 384; // 8 softmax warps (2 slots x 4), TMA warp, MMA warp, 2 V converters
 
 enum AttnMode : int { MODE_CAUSAL = 0, MODE_MASK = 1, MODE_SPARSE = 2 };
 
@@ -17,7 +17,8 @@ struct AttnArgs {
   int slots;            // query heads per CTA sharing one K/V stream (1 or 2)
   int n_hp;             // head groups of `slots` heads per batch
   int n_hist_tiles;     // key tiles served by the history map (s / 128)
-  int ab_type;          // 0 = f16, 1 = bf16 operands
+  int ab_type;          // 0 = f16, 1 = bf16 operands of S = Q K^T
+  int convert_v;        // 1: V tiles are bf16 and are converted to fp16 in shared memory
   float scale_log2;     // scale * log2(e)
   // explicit additive mask (MODE_MASK)
   const void* mask;

@@ -9,6 +9,7 @@
 
 #include "kernels.cuh"
 #include "pf.h"
+#include "ptx.cuh"
 
 namespace pf {
 thread_local long long t_launches = 0;
@@ -147,6 +148,7 @@ void fill_attn_common(const pf_shape* sh, int32_t start_pos, AttnArgs& a) {
   a.slots = (a.G % 2 == 0) ? 2 : 1;
   a.n_hp = sh->Hq / a.slots;
   a.ab_type = sh->in_dtype == PF_BF16 ? 1 : 0;
+  a.convert_v = a.ab_type;
   const float scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)sh->d);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out_dtype = sh->out_dtype == PF_F32 ? 2 : (sh->out_dtype == PF_BF16 ? 1 : 0);
@@ -182,6 +184,9 @@ pf_status pf_stream_status(void* stream) {
   if (w[0] == 0) return PF_OK;
   const unsigned zero[2] = {0, 0};
   cudaMemcpyToSymbol(g_status, zero, sizeof(zero));
+  if ((w[0] & ST_TIMEOUT) == 0u && (w[0] & ST_VRANGE) != 0u)
+    return fail(PF_ERANGE, "v holds a bf16 value outside the fp16 range of the P*V product "
+                           "(|v| > 65504, inf or nan)");
   return fail(PF_ETIMEOUT, "a bounded device wait gave up (status 0x%x, role %u, barrier %u)", w[0],
               w[1] >> 8, w[1] & 0xFFu);
 }

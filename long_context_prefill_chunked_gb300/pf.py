@@ -22,9 +22,10 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpf.so")
 
-PF_OK, PF_EINVAL, PF_EUNSUPPORTED, PF_ECUDA, PF_ETIMEOUT = range(5)
+PF_OK, PF_EINVAL, PF_EUNSUPPORTED, PF_ECUDA, PF_ETIMEOUT, PF_ERANGE = range(6)
 PF_F16, PF_BF16, PF_F32 = range(3)
-STATUS_NAMES = {0: "PF_OK", 1: "PF_EINVAL", 2: "PF_EUNSUPPORTED", 3: "PF_ECUDA", 4: "PF_ETIMEOUT"}
+STATUS_NAMES = {0: "PF_OK", 1: "PF_EINVAL", 2: "PF_EUNSUPPORTED", 3: "PF_ECUDA", 4: "PF_ETIMEOUT",
+                5: "PF_ERANGE"}
 
 EXPORTS = ["pf_attn_dense", "pf_block_index", "pf_attn_sparse", "pf_sparse_query_sizes",
            "pf_stream_status", "pf_set_wait_timeout", "pf_set_debug_withhold", "pf_launch_count",

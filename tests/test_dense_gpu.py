@@ -6,6 +6,7 @@ import torch
 import oracle
 import prefill_inputs as pi
 from gpu_util import assert_close, dev, errors, sample_rows, MAX_ABS
+from long_context_prefill_chunked_gb300 import pf
 
 pytestmark = pytest.mark.gpu
 
@@ -152,3 +153,17 @@ def test_launch_counter_counts_kernels():
     pfx.launch_count(reset=True)
     run_chunk(w, 0, None, out_kv=True)
     assert pfx.launch_count() == 3      # attention + two cache-layout copies
+
+
+def test_value_outside_fp16_range_is_reported():
+    """P * V runs in fp16; a bf16 v beyond +-65504 must be refused loudly, not rounded to inf."""
+    w = pi.normal_workload("vrange", 15, 1, 4, 2, 128, 256, 256, "bf16")
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(0))
+    vc[0, 17, 1, 5] = 1.0e6
+    pfx.attn_dense(q, kh, vh, kc, vc, 0)
+    with pytest.raises(pfx.PFError) as e:
+        pfx.stream_status()
+    assert e.value.status == pf.PF_ERANGE
+    vc[0, 17, 1, 5] = 1.0
+    pfx.attn_dense(q, kh, vh, kc, vc, 0)
+    pfx.stream_status()
