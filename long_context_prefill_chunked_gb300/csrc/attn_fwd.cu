@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     n_tiles = n_pool + *n_ex_slot;
   }
 
-  // 384 threads x 168 registers at launch; the softmax warpgroups take 224,
-  // the producer/MMA/converter warpgroup keeps 56: 2*128*224 + 128*56 = 384*168.
+  // 384 threads x 168 registers at launch; the softmax warpgroups take 216,
+  // the producer/MMA/converter warpgroup keeps 72: 2*128*216 + 128*72 = 384*168.
   if (warp >= 8) {
     regs_dec<72>();
   if (warp == 8) {
