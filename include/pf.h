@@ -154,6 +154,37 @@ pf_status pf_attn_sparse(const pf_shape* shape, const void* q, const void* k, co
                          int32_t start_pos, int32_t block, const pf_sel* sel, void* pooled,
                          void* out, void* stream);
 
+/*
+ * pf_attn_sparse_static -- pf_attn_sparse for callers that cannot allocate
+ * device memory.  The pages describe no counterpart of this entry point.
+ *
+ * Some callers have no way to give pf_attn_sparse its `pooled` workspace: a
+ * plug-in inside a host framework that owns every device allocation and hands
+ * the plug-in only its inputs and outputs, or a latency-critical serving loop
+ * that must not call cudaMalloc (it can block on the device and costs far more
+ * than the attention call).  This entry point takes the same arguments minus
+ * `pooled` and computes the same output; its scratch is a static device buffer
+ * of PF_STATIC_SCRATCH_BYTES inside libpf, resident on every GPU that loads the
+ * library until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   - Limit: a problem whose pf_sparse_query_sizes().pooled_bytes exceeds
+ *     PF_STATIC_SCRATCH_BYTES (B * Hkv * nblk * d * 8 bytes, rounded) is
+ *     rejected with PF_EUNSUPPORTED and a message in pf_last_error().
+ *   - Set-up: the first call on each device looks up the buffer's device
+ *     address (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture.
+ *   - Sharing: every call uses the same buffer, which keeps the previous call's
+ *     contents; nothing in it needs to start at zero (each call writes what it
+ *     reads).  Calls that overlap on the GPU (other streams, other host threads)
+ *     race on the buffer: order them.
+ *   - The pooled block means stay internal (no vbar output).
+ */
+#define PF_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void* k,
+                                const void* v, int32_t start_pos, int32_t block,
+                                const pf_sel* sel, void* out, void* stream);
+
 /* Synchronise `stream`, then report (and clear) a device-side error: PF_ETIMEOUT
  * if a bounded wait in a kernel gave up since the last check; PF_ERANGE if a
  * bf16 v held a value the fp16 P*V product cannot represent (|v| > 65504, inf or

@@ -15,6 +15,15 @@ namespace pf {
 thread_local long long t_launches = 0;
 }  // namespace pf
 
+namespace {
+thread_local std::string t_err;
+}
+
+namespace pf {
+// Lets other translation units of the library report through pf_last_error().
+void set_error_message(const char* msg) { t_err = msg; }
+}  // namespace pf
+
 // Device status words written by the kernels' bounded waits: [0] flags, [1] where.
 static __device__ unsigned int g_status[2];
 
@@ -22,7 +31,6 @@ using namespace pf;
 
 namespace {
 
-thread_local std::string t_err;
 long long g_timeout = 400000000LL;  // ~0.2 s at 2 GHz; legitimate waits take microseconds
 int g_withhold = 0;
 

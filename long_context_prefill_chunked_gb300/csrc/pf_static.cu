@@ -1,0 +1,91 @@
+// pf_attn_sparse_static: the block-sparse attention entry point for callers
+// that cannot allocate device memory.
+//
+// pf_attn_sparse needs a caller-provided workspace (`pooled`).  Some callers
+// have no way to provide one: a plug-in running inside a host framework that
+// owns every device allocation and hands the plug-in only its inputs and
+// outputs, or a latency-critical serving loop that must not call cudaMalloc
+// (it can block on the device and takes far longer than the attention call).
+// This entry point takes the same inputs and outputs but no workspace: the
+// scratch lives in the fixed-size device array below, which is part of the
+// library image and stays resident on every GPU that loads libpf until the
+// process exits.  Nothing here calls cudaMalloc, cudaFree or any allocating
+// library routine.
+#include <stdio.h>
+
+#include <mutex>
+
+#include "pf.h"
+
+namespace pf {
+void set_error_message(const char* msg);  // defined in pf_abi.cu; feeds pf_last_error()
+}
+
+namespace {
+
+// Scratch for the pooled means (fp32 vbar plus the 16-bit copies of kbar and
+// vbar).  PF_STATIC_SCRATCH_BYTES (16 MiB) covers B * Hkv * nblk * d * 8 bytes
+// up to 2^21 elements, e.g. 8 KV heads x head_dim 128 x 2048 key blocks (256K
+// keys) at batch 1.
+constexpr size_t kScratchBytes = PF_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_sparse_scratch[kScratchBytes];
+
+// Device address of g_sparse_scratch, looked up once per device with that
+// device current.  In host code the array's name is only a host-side stand-in;
+// kernels must be given this address instead.
+std::mutex g_mu;
+void* g_addr[64] = {nullptr};
+
+pf_status scratch_address(void** out, const char** why) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *why = "no current CUDA device";
+    return PF_ECUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_sparse_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      *why = "cudaGetSymbolAddress failed for the static scratch buffer";
+      return PF_ECUDA;
+    }
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return PF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void* k, const void* v,
+                                int32_t start_pos, int32_t block, const pf_sel* sel, void* out,
+                                void* stream) {
+  pf_sparse_sizes z;
+  pf_status rc = pf_sparse_query_sizes(shape, start_pos, block, &z);
+  if (rc != PF_OK) return rc;
+  if (z.pooled_bytes < 0 || (size_t)z.pooled_bytes > kScratchBytes) {
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "pf_attn_sparse_static: this problem needs %lld bytes of scratch but the static buffer "
+             "holds %zu; use pf_attn_sparse with a caller-allocated workspace",
+             (long long)z.pooled_bytes, kScratchBytes);
+    pf::set_error_message(msg);
+    return PF_EUNSUPPORTED;
+  }
+  void* scratch = nullptr;
+  const char* why = nullptr;
+  if ((rc = scratch_address(&scratch, &why)) != PF_OK) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "pf_attn_sparse_static: %s", why);
+    pf::set_error_message(msg);
+    return rc;
+  }
+  // Every byte of the workspace that the kernels read is written earlier in
+  // the same call, so stale contents from a previous call do not matter.
+  return pf_attn_sparse(shape, q, k, v, start_pos, block, sel, scratch, out, stream);
+}
+
+}  // extern "C"
