@@ -164,6 +164,11 @@ def test_value_outside_fp16_range_is_reported():
     with pytest.raises(pfx.PFError) as e:
         pfx.stream_status()
     assert e.value.status == pf.PF_ERANGE
+    vc[0, 17, 1, 5] = float("nan")
+    pfx.attn_dense(q, kh, vh, kc, vc, 0)
+    with pytest.raises(pfx.PFError) as e:
+        pfx.stream_status()
+    assert e.value.status == pf.PF_ERANGE
     vc[0, 17, 1, 5] = 1.0
     pfx.attn_dense(q, kh, vh, kc, vc, 0)
     pfx.stream_status()
