@@ -37,25 +37,25 @@
 namespace pf {
 namespace {
 
-constexpr int NST = 2;                               // K/V ring stages
+constexpr int NSK = 2;                               // K ring stages
+constexpr int NSV = 3;                               // V ring stages (V also waits for conversion)
 constexpr uint32_t SM_Q = 0;                         // slot s: +32 KB * s (two 64-column boxes)
 constexpr uint32_t SM_K = 65536;                     // stage st: +32 KB * st
-constexpr uint32_t SM_V = SM_K + NST * 32768;
-constexpr uint32_t SM_BAR = SM_V + NST * 32768;      // mbarriers, TMEM address, abort flag
-constexpr uint32_t SM_SEQ = SM_BAR + 256;            // sparse: merged key-block sequence
+constexpr uint32_t SM_V = SM_K + NSK * 32768;
+constexpr uint32_t SM_BAR = SM_V + NSV * 32768;      // mbarriers, TMEM address, abort flag
 constexpr int kMaxBlocks = 2048;                     // sparse: key blocks per sequence (256K keys)
-constexpr uint32_t SM_BM = SM_SEQ + kMaxBlocks * 4;  // sparse: union bitmap
+constexpr uint32_t SM_BM = SM_BAR + 256;             // sparse: union bitmap of kept key blocks
 constexpr uint32_t SM_BYTES = SM_BM + kMaxBlocks / 8 + 16;
 constexpr uint32_t SM_ALLOC = SM_BYTES + 1024;       // slack for 1024-byte alignment
 
 enum {
   B_Q = 0,
-  B_KF = 1,             // K tile landed, per stage
-  B_VF = B_KF + NST,    // V tile landed, per stage
-  B_VC = B_VF + NST,    // V tile converted to fp16 (bf16 inputs), per stage
-  B_KE = B_VC + NST,    // K stage free again (both slots' S MMAs done)
-  B_VE = B_KE + NST,    // V stage free again (both slots' PV MMAs done)
-  B_SF = B_VE + NST,    // S ready, per slot
+  B_KF = 1,             // K tile landed, per K stage
+  B_VF = B_KF + NSK,    // V tile landed, per V stage
+  B_VC = B_VF + NSV,    // V tile converted to fp16 (bf16 inputs), per V stage
+  B_KE = B_VC + NSV,    // K stage free again (both slots' S MMAs done)
+  B_VE = B_KE + NSK,    // V stage free again (both slots' PV MMAs done)
+  B_SF = B_VE + NSV,    // S ready, per slot
   B_PF = B_SF + 2,      // P written (and O rescaled), per slot
   B_OF = B_PF + 2,      // last PV done
   B_DR = B_OF + 1,      // drain: all issued MMAs done
@@ -92,6 +92,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
   }
 }
 
+// Walks the set bits of the kept-block bitmap in ascending order.
+struct BlockWalk {
+  const uint32_t* bm;
+  int w;
+  uint32_t rb;
+  __device__ void init(const uint32_t* bitmap) { bm = bitmap; w = 0; rb = bitmap[0]; }
+  __device__ int next() {
+    while (rb == 0u) rb = bm[++w];
+    const int t = __ffs(rb) - 1;
+    rb &= rb - 1u;
+    return w * 32 + t;
+  }
+};
+
 __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&x)[128]) {
   uint32_t r[128];
   tmem_ld128_wait(taddr, r);
@@ -112,7 +126,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_BAR + 8 * N_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_BAR + 8 * N_BARS + 4);
   int* n_ex_slot = reinterpret_cast<int*>(smem + SM_BAR + 8 * N_BARS + 8);
-  int* seq = reinterpret_cast<int*>(smem + SM_SEQ);
+  const uint32_t* kept_bm = reinterpret_cast<const uint32_t*>(smem + SM_BM);
 
   // ---- work unit: heaviest query tiles first (longest causal key range)
   const int per_qt = a.n_hp * a.B;
@@ -126,11 +140,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_Q), 1);
-    for (int st = 0; st < NST; ++st) {
+    for (int st = 0; st < NSK; ++st) {
       mbar_init(BAR(B_KF + st), 1);
+      mbar_init(BAR(B_KE + st), 1);
+    }
+    for (int st = 0; st < NSV; ++st) {
       mbar_init(BAR(B_VF + st), 1);
       mbar_init(BAR(B_VC + st), kConvWarps);
-      mbar_init(BAR(B_KE + st), 1);
       mbar_init(BAR(B_VE + st), 1);
     }
     for (int sl = 0; sl < 2; ++sl) {
@@ -161,26 +177,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (kb >= 0 && kb < a.nblk) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
     }
     __syncwarp();
-    int base = 0;
-    for (int w0 = 0; w0 < a.words; w0 += 32) {
-      const int w = w0 + lane;
-      const uint32_t bits = (w < a.words) ? bm[w] : 0u;
-      const int cnt = __popc(bits);
-      int incl = cnt;
+    int cnt = 0;
+    for (int w = lane; w < a.words; w += 32) cnt += __popc(bm[w]);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      int pos = base + incl - cnt;
-      uint32_t rb = bits;
-      while (rb) {
-        const int t = __ffs(rb) - 1;
-        rb &= rb - 1u;
-        seq[pos++] = w * 32 + t;
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    const int base = cnt;
     if (lane == 0) *n_ex_slot = base;
   }
   if (warp == 9) {
@@ -211,8 +212,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       const int nd = a.d / 64;
       const uint32_t tile_bytes = (uint32_t)nd * 16384u;
-      int last_use[NST];
-      for (int st = 0; st < NST; ++st) last_use[st] = -1;
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.kh);
       tma_prefetch_desc(&maps.vh);
@@ -221,10 +220,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < nd; ++c)
           tma_load_4d(sb + SM_Q + 32768u * sl + 16384u * c, &maps.q, BAR(B_Q), 64 * c, h0 + sl,
                       q0, b);
-      int last_k[NST], last_v[NST];
-      for (int st = 0; st < NST; ++st) last_k[st] = last_v[st] = -1;
+      int last_k[NSK], last_v[NSV];
+      for (int st = 0; st < NSK; ++st) last_k[st] = -1;
+      for (int st = 0; st < NSV; ++st) last_v[st] = -1;
+      BlockWalk walk;
+      if (MODE == MODE_SPARSE) walk.init(kept_bm);
       for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % NST, use = j / NST;
+        const int st = j % NSK, use = j / NSK;
+        const int sv = j % NSV, usev = j / NSV;
         const CUtensorMap *mk, *mv;
         int c1, c2;
         if (MODE == MODE_SPARSE && j < n_pool) {
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           c1 = j * kTile;
           c2 = g;
         } else {
-          const int kt = (MODE == MODE_SPARSE) ? seq[j - n_pool] : j;
+          const int kt = (MODE == MODE_SPARSE) ? walk.next() : j;
           if (kt < a.n_hist_tiles) {
             mk = &maps.kh;
             mv = &maps.vh;
@@ -252,20 +255,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < nd; ++c)
           tma_load_4d(sb + SM_K + 32768u * st + 16384u * c, mk, BAR(B_KF + st), 64 * c, c1, c2, b);
         last_k[st] = use;
-        if (use > 0 && !mbar_wait(BAR(B_VE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
-                                  (R_PROD << 8) | (B_VE + st)))
+        if (usev > 0 && !mbar_wait(BAR(B_VE + sv), (usev - 1) & 1, a.timeout, abort_flag, a.status,
+                                   (R_PROD << 8) | (B_VE + sv)))
           break;
-        mbar_arrive_expect_tx(BAR(B_VF + st), tile_bytes);
+        mbar_arrive_expect_tx(BAR(B_VF + sv), tile_bytes);
         for (int c = 0; c < nd; ++c)
-          tma_load_4d(sb + SM_V + 32768u * st + 16384u * c, mv, BAR(B_VF + st), 64 * c, c1, c2, b);
-        last_v[st] = use;
+          tma_load_4d(sb + SM_V + 32768u * sv + 16384u * c, mv, BAR(B_VF + sv), 64 * c, c1, c2, b);
+        last_v[sv] = usev;
       }
       if (*abort_flag) {  // let this warp's copies land before the CTA exits
         drain_wait(BAR(B_Q), 0, a.timeout, a.status);
-        for (int st = 0; st < NST; ++st) {
+        for (int st = 0; st < NSK; ++st)
           if (last_k[st] >= 0) drain_wait(BAR(B_KF + st), last_k[st] & 1, a.timeout, a.status);
+        for (int st = 0; st < NSV; ++st)
           if (last_v[st] >= 0) drain_wait(BAR(B_VF + st), last_v[st] & 1, a.timeout, a.status);
-        }
       }
     }
     __syncwarp();
@@ -303,8 +306,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = mbar_wait(BAR(B_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | B_Q);
       tc_fence_after();
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % NST;
-        const uint32_t ph = (uint32_t)(j / NST) & 1u;
+        const int st = j % NSK;
+        const uint32_t ph = (uint32_t)(j / NSK) & 1u;
+        const int sv = j % NSV;
+        const uint32_t phv = (uint32_t)(j / NSV) & 1u;
         if (j == 0) {
           ok = mbar_wait(BAR(B_KF + st), ph, a.timeout, abort_flag, a.status, (R_MMA << 8) | (B_KF + st));
           if (!ok) break;
@@ -315,20 +320,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           tc_commit(BAR(B_KE + st));
         }
-        ok = mbar_wait(BAR(vbar_first + st), ph, a.timeout, abort_flag, a.status,
-                       (R_MMA << 8) | (vbar_first + st));
+        ok = mbar_wait(BAR(vbar_first + sv), phv, a.timeout, abort_flag, a.status,
+                       (R_MMA << 8) | (vbar_first + sv));
         if (!ok) break;
         tc_fence_after();
-        const int st1 = (j + 1) % NST;
+        const int st1 = (j + 1) % NSK;
         for (int sl = 0; sl < a.slots; ++sl) {
           ok = mbar_wait(BAR(B_PF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
                          (R_MMA << 8) | (B_PF + sl));
           if (!ok) break;
           tc_fence_after();
-          issue_pv(sl, st, j > 0);
+          issue_pv(sl, sv, j > 0);
           if (j + 1 < n_tiles) {
             if (sl == 0) {
-              ok = mbar_wait(BAR(B_KF + st1), (uint32_t)((j + 1) / NST) & 1u, a.timeout,
+              ok = mbar_wait(BAR(B_KF + st1), (uint32_t)((j + 1) / NSK) & 1u, a.timeout,
                              abort_flag, a.status, (R_MMA << 8) | (B_KF + st1));
               if (!ok) break;
               tc_fence_after();
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (!ok) break;
         if (j + 1 < n_tiles) tc_commit(BAR(B_KE + st1));
-        tc_commit(BAR(B_VE + st));
+        tc_commit(BAR(B_VE + sv));
       }
       if (ok) tc_commit(BAR(B_OF));
       tc_commit(BAR(B_DR));  // no MMA may still run when tensor memory is released
@@ -352,8 +357,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int nvec = (a.d / 64) * 1024;  // 16-byte vectors per V tile
     float vmax = 0.f;                    // largest |v| seen (bf16 values are exact in fp32)
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % NST;
-      if (!wait_all(BAR(B_VF + st), (uint32_t)(j / NST) & 1u, a.timeout, abort_flag, a.status,
+      const int st = j % NSV;
+      if (!wait_all(BAR(B_VF + st), (uint32_t)(j / NSV) & 1u, a.timeout, abort_flag, a.status,
                     (R_CONV << 8) | (B_VF + st)))
         break;
       uint4* v = reinterpret_cast<uint4*>(smem + SM_V + 32768u * st);
@@ -394,6 +399,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bits_row = a.row_bits + ((long long)(b * a.Hq + h) * a.C + row) * a.words;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    BlockWalk walk;
+    if (MODE == MODE_SPARSE) walk.init(kept_bm);
     for (int j = 0; j < n_tiles; ++j) {
       ok = wait_all(BAR(B_SF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
                     (R_SOFT << 8) | (B_SF + sl));
@@ -486,7 +493,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
         } else {
-          const int kb = seq[j - n_pool];
+          const int kb = walk.next();
           if (kb == ob) {
 #pragma unroll
             for (int c = 0; c < 128; ++c)
