@@ -115,10 +115,13 @@ typedef struct {
   uint32_t* row_bits;  /* [B, Hq, C, W]: bit (b % 32) of word b / 32 set iff the row keeps block b */
   int32_t* tile_list;  /* [B, Hq, nqt, nblk]: ascending union of the kept blocks of the tile's rows */
   int32_t* tile_cnt;   /* [B, Hq, nqt]: valid entries of tile_list */
-  float* kbar;         /* [B, Hkv, nblk, d]: pooled (mean) keys, fp32 */
+  float* kbar;         /* 2 * B*Hkv*nblk*d floats: the fp32 pooled (mean) keys [B, Hkv, nblk, d],
+                          then the library's 16-bit split of them (hi = round(mean), lo =
+                          round(mean - hi), each [B, Hkv, nblk, d] in the q/k type) */
 } pf_sel;
 
-/* Element counts of the pf_sel buffers and of the pf_attn_sparse workspace. */
+/* Element counts of the pf_sel buffers (kbar_elems counts floats) and the byte size of
+ * the pf_attn_sparse workspace. */
 typedef struct {
   int64_t nblk, nqt, words;
   int64_t row_bits_elems, tile_list_elems, tile_cnt_elems, kbar_elems;

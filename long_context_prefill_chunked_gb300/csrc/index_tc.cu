@@ -1,0 +1,303 @@
+// Block index on the tensor cores: pooled scores s_rb = q_r . kbar_b for every
+// query row and every earlier key block, the row's hottest block, and the kept
+// blocks (exp(s_rb - s_max) >= alpha, i.e. (s_rb - s_max) * scale >= ln alpha)
+// plus the diagonal; then each query tile's union of kept blocks, ascending.
+//
+// Method: "Porting FlashPrefill V2 to Apple silicon for faster prefill",
+// sections "A cheap map of where the attention lives" (one pooled score per
+// query row per block, local block exact) and "The algorithm starts here"
+// (keep blocks above alpha x the row's hottest block, plus the diagonal).
+//
+// The scores must decide a threshold the float64 definition decides, so they
+// are computed to about 2^-17 relative error: kbar (fp32 block means) is split
+// into kbar_hi = bf16(kbar) and kbar_lo = bf16(kbar - kbar_hi) and each score is
+// accumulated in fp32 tensor memory as q . kbar_hi + q . kbar_lo (q is bf16 and
+// exact).  Pass 1 streams every pooled tile (128 blocks) once to find the row
+// maximum, pass 2 streams them again and thresholds.
+//
+// One CTA = (batch, 128-row query tile, `slots` query heads of one KV group):
+//   warps 0-3 / 4-7  row threads of slot 0 / 1 (thread t owns row t = TMEM lane t)
+//   warp 8           TMA producer (Q once, then kbar hi/lo tiles, 2-stage ring)
+//   warp 9           MMA issuer and TMEM owner (slot s, buffer u: columns 256s + 128u)
+#include <math.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace pf {
+namespace {
+
+constexpr int XST = 2;                          // kbar tile ring stages
+constexpr uint32_t X_Q = 0;                     // slot s: +32 KB * s
+constexpr uint32_t X_K = 65536;                 // stage st: hi at +64 KB * st, lo at +32 KB
+constexpr uint32_t X_BAR = X_K + XST * 65536;   // barriers, TMEM address, abort flag
+constexpr uint32_t X_UNI = X_BAR + 256;         // per-slot union bitmaps, 64 words each
+constexpr uint32_t X_BYTES = X_UNI + 2 * 256 + 16;
+constexpr uint32_t X_ALLOC = X_BYTES + 1024;
+constexpr int kIndexThreads = 320;
+constexpr int kMaxWords = 64;
+
+enum {
+  I_Q = 0,
+  I_KF = 1,            // hi/lo tile landed, per stage
+  I_KE = I_KF + XST,   // stage free (both slots' MMAs on it done)
+  I_SF = I_KE + XST,   // score buffer full, per (slot, buffer)
+  I_SE = I_SF + 4,     // score buffer drained by the row threads, per (slot, buffer)
+  I_DR = I_SE + 4,
+  I_N = I_DR + 1
+};
+enum { R_PROD = 1, R_MMA = 2, R_ROW = 3 };
+
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, long long timeout,
+                                         volatile int* abort_flag, unsigned* status,
+                                         unsigned where) {
+  bool ok = mbar_wait(bar, parity, timeout, abort_flag, status, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long timeout,
+                                           unsigned* status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > timeout) {
+      record_error(status, ST_TIMEOUT, 0xFEu);
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kIndexThreads, 1)
+    index_tc_kernel(const __grid_constant__ IndexMaps maps, const IndexArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = sb + X_BAR;
+#define XB(i) (bar0 + 8u * (uint32_t)(i))
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + X_BAR + 8 * I_N);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + X_BAR + 8 * I_N + 4);
+  uint32_t* uni = reinterpret_cast<uint32_t*>(smem + X_UNI);  // [slot][64]
+
+  const int per_qt = a.n_hp * a.B;
+  const int qt = a.n_qt - 1 - (int)blockIdx.x / per_qt;
+  const int rem = (int)blockIdx.x % per_qt;
+  const int b = rem / a.n_hp;
+  const int h0 = (rem % a.n_hp) * a.slots;
+  const int g = h0 / a.G;
+  const int q0 = qt * kTile;
+  const int ob = (a.s + q0) / kTile;           // diagonal block; candidates 0 .. ob-1
+  const int np = (ob + kTile - 1) / kTile;     // pooled tiles holding the candidates
+  const int nsteps = 2 * np;                   // pass 1 and pass 2
+
+  if (threadIdx.x == 0) {
+    mbar_init(XB(I_Q), 1);
+    for (int st = 0; st < XST; ++st) {
+      mbar_init(XB(I_KF + st), 1);
+      mbar_init(XB(I_KE + st), 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(XB(I_SF + i), 1);
+      mbar_init(XB(I_SE + i), 4);
+    }
+    mbar_init(XB(I_DR), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < 2 * kMaxWords; i += blockDim.x) uni[i] = 0u;
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && nsteps > 0) {
+      const int nd = a.d / 64;
+      const uint32_t box = 16384u;
+      int last[XST] = {-1, -1};
+      mbar_arrive_expect_tx(XB(I_Q), box * nd * (uint32_t)a.slots);
+      for (int sl = 0; sl < a.slots; ++sl)
+        for (int c = 0; c < nd; ++c)
+          tma_load_4d(sb + X_Q + 32768u * sl + box * c, &maps.q, XB(I_Q), 64 * c, h0 + sl, q0, b);
+      for (int t = 0; t < nsteps; ++t) {
+        const int st = t % XST, use = t / XST;
+        const int pt = t % np;
+        if (use > 0 && !mbar_wait(XB(I_KE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
+                                  (R_PROD << 8) | (I_KE + st)))
+          break;
+        mbar_arrive_expect_tx(XB(I_KF + st), 2u * box * nd);
+        for (int c = 0; c < nd; ++c) {
+          tma_load_4d(sb + X_K + 65536u * st + box * c, &maps.hi, XB(I_KF + st), 64 * c, pt * kTile, g, b);
+          tma_load_4d(sb + X_K + 65536u * st + 32768u + box * c, &maps.lo, XB(I_KF + st), 64 * c,
+                      pt * kTile, g, b);
+        }
+        last[st] = use;
+      }
+      if (*abort_flag) {
+        drain_wait(XB(I_Q), 0, a.timeout, a.status);
+        for (int st = 0; st < XST; ++st)
+          if (last[st] >= 0) drain_wait(XB(I_KF + st), last[st] & 1, a.timeout, a.status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nsteps > 0) {
+      const uint32_t idesc = make_idesc_f16((uint32_t)a.ab_type, 128, 128, 0);  // -> fp32
+      const int kq = a.d / 16;
+      const uint64_t dq0 = make_sdesc_sw128(sb + X_Q, 16, 1024);
+      const uint64_t dk0 = make_sdesc_sw128(sb + X_K, 16, 1024);
+      bool ok = mbar_wait(XB(I_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | I_Q);
+      tc_fence_after();
+      for (int t = 0; ok && t < nsteps; ++t) {
+        const int st = t % XST, u = t % 2;
+        ok = mbar_wait(XB(I_KF + st), (uint32_t)(t / XST) & 1u, a.timeout, abort_flag, a.status,
+                       (R_MMA << 8) | (I_KF + st));
+        if (!ok) break;
+        for (int sl = 0; sl < a.slots; ++sl) {
+          if (t >= 2) {
+            ok = mbar_wait(XB(I_SE + 2 * sl + u), (uint32_t)(t / 2 - 1) & 1u, a.timeout, abort_flag,
+                           a.status, (R_MMA << 8) | (I_SE + 2 * sl + u));
+            if (!ok) break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + 256u * sl + 128u * u;
+          const uint64_t aq = dq0 + ((32768u * sl) >> 4);
+          const uint64_t bh = dk0 + ((65536u * st) >> 4);
+          const uint64_t bl = dk0 + ((65536u * st + 32768u) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            if (kk < kq) {
+              const uint32_t off = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+              mma_ss(d_tmem, aq + off, bh + off, idesc, kk > 0 ? 1u : 0u);
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            if (kk < kq) {
+              const uint32_t off = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+              mma_ss(d_tmem, aq + off, bl + off, idesc, 1u);
+            }
+          }
+          tc_commit(XB(I_SF + 2 * sl + u));
+        }
+        if (!ok) break;
+        tc_commit(XB(I_KE + st));
+      }
+      tc_commit(XB(I_DR));
+      drain_wait(XB(I_DR), 0, a.timeout, a.status);
+    }
+    __syncwarp();
+  } else if ((warp >> 2) < a.slots) {
+    // ---------------------------------------------------------------- row threads
+    const int sl = warp >> 2, quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int h = h0 + sl;
+    const int row = q0 + r;
+    const bool valid = row < a.C;
+    uint32_t* bits = a.row_bits + ((long long)(b * a.Hq + h) * a.C + (valid ? row : 0)) * a.words;
+    uint32_t* un = uni + kMaxWords * sl;
+    const int dword = ob >> 5;
+    const uint32_t dbit = 1u << (ob & 31);
+    float smax = -INFINITY;
+    bool ok = true;
+    for (int t = 0; t < nsteps; ++t) {
+      const int u = t % 2, pass = t / np, pt = t % np;
+      ok = wait_all(XB(I_SF + 2 * sl + u), (uint32_t)(t / 2) & 1u, a.timeout, abort_flag, a.status,
+                    (R_ROW << 8) | (I_SF + 2 * sl + u));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t xr[128];
+      tmem_ld128_wait(tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl + 128u * u, xr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(XB(I_SE + 2 * sl + u));
+      const int lim = ob - pt * kTile;  // columns c < lim are candidates
+      if (pass == 0) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < lim) smax = fmaxf(smax, __uint_as_float(xr[c]));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t word = 0u;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 32 * q + i;
+            if (c < lim && (__uint_as_float(xr[c]) - smax) * a.scale >= a.log_alpha) word |= 1u << i;
+          }
+          const int w = pt * 4 + q;
+          if (w == dword) word |= dbit;
+          if (w < a.words) {
+            if (valid) bits[w] = word;
+            const uint32_t uw = __reduce_or_sync(0xffffffffu, valid ? word : 0u);
+            if (lane == 0 && uw) atomicOr(&un[w], uw);
+          }
+        }
+      }
+    }
+    if (ok) {
+      // words past the pooled tiles: only the diagonal bit
+      for (int w = 4 * np; w < a.words; ++w) {
+        const uint32_t word = (w == dword) ? dbit : 0u;
+        if (valid) bits[w] = word;
+      }
+      if (r == 0) atomicOr(&un[dword], dbit);
+    }
+    // the slot's four row warps finish their unions before warp 0 of the slot compacts
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + sl) : "memory");
+    if (quad == 0 && ok) {
+      const long long tl = (long long)(b * a.Hq + h) * a.n_qt + qt;
+      int32_t* list = a.tile_list + tl * a.nblk;
+      int base = 0;
+      for (int w0 = 0; w0 < a.words; w0 += 32) {
+        const int w = w0 + lane;
+        const uint32_t bw = (w < a.words) ? un[w] : 0u;
+        const int cnt = __popc(bw);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        int pos = base + incl - cnt;
+        uint32_t rb = bw;
+        while (rb) {
+          const int i = __ffs(rb) - 1;
+          rb &= rb - 1u;
+          list[pos++] = w * 32 + i;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) a.tile_cnt[tl] = base;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+#undef XB
+}
+
+}  // namespace
+
+cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         X_ALLOC);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = a.n_qt * a.n_hp * a.B;
+  index_tc_kernel<<<grid, kIndexThreads, X_ALLOC, st>>>(maps, a);
+  ++t_launches;
+  return cudaGetLastError();
+}
+
+}  // namespace pf

@@ -59,23 +59,28 @@ struct PoolArgs {
   long long sb, st, sh;
   float* out_f32;        // [B, H, nblk, d]
   void* out_lp;          // [B, H, nblk, d] in the input type, may be null
+  void* out_hi;          // [B, H, nblk, d] 16-bit round of the mean, may be null
+  void* out_lo;          // [B, H, nblk, d] 16-bit round of (mean - hi), may be null
 };
 cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st);
 cudaError_t launch_f32_to_lp(const float* src, void* dst, long long n, int bf16, cudaStream_t st);
 
 struct IndexArgs {
-  const void* q;
-  int ab_type;
+  int ab_type;           // 0 = f16, 1 = bf16 (q and the kbar hi/lo split)
   int B, Hq, Hkv, G, d, C, s, nblk, n_qt, words;
-  long long q_sb, q_st, q_sh;
-  const float* kbar;     // [B, Hkv, nblk, d]
+  int slots, n_hp;       // query heads per CTA (1 or 2) and head groups per batch
   float scale;
   float log_alpha;       // ln(alpha); -inf when alpha == 0
   uint32_t* row_bits;
   int32_t* tile_list;
   int32_t* tile_cnt;
+  unsigned* status;
+  long long timeout;
 };
-cudaError_t launch_index(const IndexArgs& a, cudaStream_t st);
+struct IndexMaps {
+  CUtensorMap q, hi, lo;
+};
+cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st);
 
 extern thread_local long long t_launches;
 

@@ -288,9 +288,10 @@ pf_status pf_sparse_query_sizes(const pf_shape* sh, int32_t start_pos, int32_t b
   z->row_bits_elems = (long long)sh->B * sh->Hq * sh->C * z->words;
   z->tile_list_elems = (long long)sh->B * sh->Hq * z->nqt * z->nblk;
   z->tile_cnt_elems = (long long)sh->B * sh->Hq * z->nqt;
-  z->kbar_elems = (long long)sh->B * sh->Hkv * z->nblk * sh->d;
-  const long long f32b = (z->kbar_elems * 4 + 255) / 256 * 256;
-  const long long lpb = (z->kbar_elems * 2 + 255) / 256 * 256;
+  const long long pe = (long long)sh->B * sh->Hkv * z->nblk * sh->d;  // pooled elements
+  z->kbar_elems = 2 * pe;  // fp32 means, then the 16-bit hi and lo split of them
+  const long long f32b = (pe * 4 + 255) / 256 * 256;
+  const long long lpb = (pe * 2 + 255) / 256 * 256;
   z->pooled_bytes = f32b + 2 * lpb;
   return PF_OK;
 }
@@ -328,44 +329,59 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
     return fail(PF_EINVAL, "q, k and kbar must be 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = start_pos + sh->C;
+  const int B = sh->B, Hkv = sh->Hkv, d = sh->d, nblk = (int)z.nblk;
+  const long long pe = z.kbar_elems / 2;
+  uint16_t* kb_hi = reinterpret_cast<uint16_t*>(sel->kbar + pe);
+  uint16_t* kb_lo = kb_hi + pe;
   PoolArgs p{};
   p.x = k;
-  p.B = sh->B;
+  p.B = B;
   p.T = T;
-  p.H = sh->Hkv;
-  p.d = sh->d;
+  p.H = Hkv;
+  p.d = d;
   p.block = block;
-  p.nblk = (int)z.nblk;
+  p.nblk = nblk;
   p.sb = ks[0];
   p.st = ks[1];
   p.sh = ks[2];
   p.out_f32 = sel->kbar;
   p.out_lp = nullptr;
+  p.out_hi = kb_hi;
+  p.out_lo = kb_lo;
   cudaError_t e = launch_pool(p, sh->in_dtype == PF_BF16 ? 1 : 0, st);
   if (e != cudaSuccess) return cuda_fail(e, "pool launch");
   IndexArgs ia{};
-  ia.q = q;
   ia.ab_type = sh->in_dtype == PF_BF16 ? 1 : 0;
-  ia.B = sh->B;
+  ia.B = B;
   ia.Hq = sh->Hq;
-  ia.Hkv = sh->Hkv;
-  ia.G = sh->Hq / sh->Hkv;
-  ia.d = sh->d;
+  ia.Hkv = Hkv;
+  ia.G = sh->Hq / Hkv;
+  ia.d = d;
   ia.C = sh->C;
   ia.s = start_pos;
-  ia.nblk = (int)z.nblk;
+  ia.nblk = nblk;
   ia.n_qt = (int)z.nqt;
   ia.words = (int)z.words;
-  ia.q_sb = qs[0];
-  ia.q_st = qs[1];
-  ia.q_sh = qs[2];
-  ia.kbar = sel->kbar;
-  ia.scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)sh->d);
+  ia.slots = (ia.G % 2 == 0) ? 2 : 1;
+  ia.n_hp = sh->Hq / ia.slots;
+  ia.scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)d);
   ia.log_alpha = alpha > 0.f ? logf(alpha) : -INFINITY;
   ia.row_bits = sel->row_bits;
   ia.tile_list = sel->tile_list;
   ia.tile_cnt = sel->tile_cnt;
-  if ((e = launch_index(ia, st)) != cudaSuccess) return cuda_fail(e, "index launch");
+  ia.status = status_words();
+  ia.timeout = g_timeout;
+  if (ia.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
+  IndexMaps maps;
+  const long long pst[3] = {(long long)Hkv * nblk * d, (long long)nblk * d, (long long)d};
+  if ((rc = map_tokens(&maps.q, q, sh->in_dtype, B, sh->C, sh->Hq, d, qs, "q")) != PF_OK) return rc;
+  if ((rc = make_map(&maps.hi, kb_hi, sh->in_dtype, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+                     "kbar hi")) != PF_OK)
+    return rc;
+  if ((rc = make_map(&maps.lo, kb_lo, sh->in_dtype, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+                     "kbar lo")) != PF_OK)
+    return rc;
+  if ((e = launch_index(maps, ia, st)) != cudaSuccess) return cuda_fail(e, "index launch");
   return PF_OK;
 }
 
@@ -387,10 +403,11 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   if (!strides_ok(os, esize(sh->out_dtype))) return fail(PF_EINVAL, "out strides must be multiples of 16 bytes");
   const int B = sh->B, C = sh->C, Hq = sh->Hq, Hkv = sh->Hkv, d = sh->d, T = start_pos + C;
   const int nblk = (int)z.nblk;
-  const long long f32b = (z.kbar_elems * 4 + 255) / 256 * 256;
-  const long long lpb = (z.kbar_elems * 2 + 255) / 256 * 256;
+  const long long pe = z.kbar_elems / 2;
+  const long long f32b = (pe * 4 + 255) / 256 * 256;
+  const long long lpb = (pe * 2 + 255) / 256 * 256;
   float* vbar = static_cast<float*>(pooled);
-  void* kbar_lp = static_cast<char*>(pooled) + f32b;
+  void* kbar_lp = sel->kbar + pe;  // the 16-bit round of the pooled keys written by pf_block_index
   void* vbar_lp = static_cast<char*>(pooled) + f32b + lpb;
   const int bf16 = sh->in_dtype == PF_BF16 ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -408,10 +425,10 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   p.sh = ks[2];
   p.out_f32 = vbar;
   p.out_lp = vbar_lp;
+  p.out_hi = nullptr;
+  p.out_lo = nullptr;
   cudaError_t e = launch_pool(p, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "pool launch");
-  if ((e = launch_f32_to_lp(sel->kbar, kbar_lp, z.kbar_elems, bf16, st)) != cudaSuccess)
-    return cuda_fail(e, "kbar conversion");
 
   AttnArgs a{};
   fill_attn_common(sh, start_pos, a);

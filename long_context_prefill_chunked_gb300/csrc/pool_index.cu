@@ -1,11 +1,6 @@
-// Block pooling and block selection for the block-sparse path.
-//
-// "Porting FlashPrefill V2 to Apple silicon for faster prefill":
-//   section "Compress keys before the heavy work"  -> pool_kernel (block means)
-//   section "A cheap map of where the attention lives" and "The algorithm
-//   starts here" -> index_kernel: one pooled score per query row per earlier
-//   block, keep the blocks within ln(alpha) of the row's hottest block plus
-//   the diagonal, and compact each query tile's union of kept blocks.
+// Block pooling for the block-sparse path ("Porting FlashPrefill V2 to Apple
+// silicon for faster prefill", section "Compress keys before the heavy work":
+// average the keys of each block into one pooled key; values likewise).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -74,6 +69,20 @@ __global__ void pool_kernel(PoolArgs a, int bf16) {
                   : pack_f16(acc[2 * k] * inv, acc[2 * k + 1] * inv);
     *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out_lp) + o) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  if (a.out_hi != nullptr) {
+    // mean = hi + lo + O(2^-17 |mean|): the index scores q.hi + q.lo to that accuracy
+    uint32_t wh[4], wl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float m0 = acc[2 * k] * inv, m1 = acc[2 * k + 1] * inv;
+      wh[k] = bf16 ? pack_bf16(m0, m1) : pack_f16(m0, m1);
+      const float h0 = bf16 ? __uint_as_float(wh[k] << 16) : __half2float(__ushort_as_half((unsigned short)(wh[k] & 0xFFFFu)));
+      const float h1 = bf16 ? __uint_as_float(wh[k] & 0xFFFF0000u) : __half2float(__ushort_as_half((unsigned short)(wh[k] >> 16)));
+      wl[k] = bf16 ? pack_bf16(m0 - h0, m1 - h1) : pack_f16(m0 - h0, m1 - h1);
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out_hi) + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out_lo) + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  }
 }
 
 __global__ void f32_to_lp_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
@@ -82,114 +91,6 @@ __global__ void f32_to_lp_kernel(const float* __restrict__ src, uint16_t* __rest
        i += (long long)gridDim.x * blockDim.x) {
     const float2 v = reinterpret_cast<const float2*>(src)[i];
     reinterpret_cast<uint32_t*>(dst)[i] = bf16 ? pack_bf16(v.x, v.y) : pack_f16(v.x, v.y);
-  }
-}
-
-constexpr int kChunk = 32;     // pooled blocks staged per step (one selection word)
-constexpr int kMaxWords = 64;  // selection words per row (2048 blocks)
-
-// One CTA per (query tile, batch, head); thread r owns query row q0 + r.
-// Pass 1 finds the row's hottest candidate, pass 2 recomputes the scores and
-// keeps b iff (s_b - s_max) * scale >= ln(alpha).
-template <int D>
-__global__ void __launch_bounds__(128) index_kernel(IndexArgs a) {
-  __shared__ float kb[kChunk][D];
-  __shared__ uint32_t uni[kMaxWords];
-  const int per_qt = a.B * a.Hq;
-  const int qt = a.n_qt - 1 - (int)blockIdx.x / per_qt;
-  const int rem = (int)blockIdx.x % per_qt;
-  const int b = rem / a.Hq, h = rem % a.Hq, g = h / a.G;
-  const int r = threadIdx.x, lane = r & 31;
-  const int q0 = qt * kTile, row = q0 + r;
-  const bool valid = row < a.C;
-  const int ob = (a.s + q0) / kTile;  // candidates: blocks 0 .. ob-1
-  for (int w = r; w < kMaxWords; w += 128) uni[w] = 0u;
-
-  float q[D];
-  {
-    const uint16_t* qp = static_cast<const uint16_t*>(a.q) + b * a.q_sb + (long long)(valid ? row : 0) * a.q_st +
-                         (long long)h * a.q_sh;
-#pragma unroll
-    for (int v = 0; v < D / 8; ++v) {
-      float f[8];
-      unpack8(valid ? __ldg(reinterpret_cast<const uint4*>(qp) + v) : make_uint4(0, 0, 0, 0),
-              a.ab_type == 1, f);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) q[8 * v + k] = f[k];
-    }
-  }
-  const float* kbar = a.kbar + ((long long)b * a.Hkv + g) * a.nblk * D;
-  float smax = -INFINITY;
-  uint32_t* bits = a.row_bits + ((long long)(b * a.Hq + h) * a.C + (valid ? row : 0)) * a.words;
-  const int dword = ob >> 5;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int c0 = 0; c0 < ob; c0 += kChunk) {
-      const int nc = min(kChunk, ob - c0);
-      __syncthreads();
-      for (int i = r; i < nc * D / 4; i += 128)
-        reinterpret_cast<float4*>(&kb[0][0])[i] = reinterpret_cast<const float4*>(kbar + (long long)c0 * D)[i];
-      __syncthreads();
-      uint32_t word = 0u;
-      for (int i = 0; i < nc; ++i) {
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int e = 0; e < D; e += 4) {
-          const float4 k4 = *reinterpret_cast<const float4*>(&kb[i][e]);
-          s0 = fmaf(q[e], k4.x, s0);
-          s1 = fmaf(q[e + 1], k4.y, s1);
-          s2 = fmaf(q[e + 2], k4.z, s2);
-          s3 = fmaf(q[e + 3], k4.w, s3);
-        }
-        const float s = (s0 + s1) + (s2 + s3);
-        if (pass == 0) {
-          smax = fmaxf(smax, s);
-        } else if ((s - smax) * a.scale >= a.log_alpha) {
-          word |= 1u << i;
-        }
-      }
-      if (pass == 1) {
-        const int w = c0 >> 5;
-        if (w == dword) word |= 1u << (ob & 31);
-        if (valid) bits[w] = word;
-        const uint32_t u = __reduce_or_sync(0xffffffffu, valid ? word : 0u);
-        if (lane == 0 && u) atomicOr(&uni[w], u);
-      }
-    }
-  }
-  // words past the last candidate chunk: only the diagonal bit can be set
-  const int w_first = (ob + kChunk - 1) / kChunk;
-  for (int w = w_first; w < a.words; ++w) {
-    const uint32_t word = (w == dword) ? (1u << (ob & 31)) : 0u;
-    if (valid) bits[w] = word;
-  }
-  __syncthreads();
-  if (r == 0) uni[dword] |= 1u << (ob & 31);
-  __syncthreads();
-  // compact the tile's union of kept blocks, ascending
-  if (r < 32) {
-    const long long t = (long long)(b * a.Hq + h) * a.n_qt + qt;
-    int32_t* list = a.tile_list + t * a.nblk;
-    int base = 0;
-    for (int w0 = 0; w0 < a.words; w0 += 32) {
-      const int w = w0 + lane;
-      const uint32_t bw = (w < a.words) ? uni[w] : 0u;
-      const int cnt = __popc(bw);
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int pos = base + incl - cnt;
-      uint32_t rb = bw;
-      while (rb) {
-        const int i = __ffs(rb) - 1;
-        rb &= rb - 1u;
-        list[pos++] = w * 32 + i;
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) a.tile_cnt[t] = base;
   }
 }
 
@@ -208,16 +109,6 @@ cudaError_t launch_f32_to_lp(const float* src, void* dst, long long n, int bf16,
   long long want = (pairs + threads - 1) / threads;
   const int grid = (int)(want < 152 * 8 ? (want > 0 ? want : 1) : 152 * 8);
   f32_to_lp_kernel<<<grid, threads, 0, st>>>(src, static_cast<uint16_t*>(dst), n, bf16);
-  ++t_launches;
-  return cudaGetLastError();
-}
-
-cudaError_t launch_index(const IndexArgs& a, cudaStream_t st) {
-  const int grid = a.n_qt * a.B * a.Hq;
-  if (a.d == 128)
-    index_kernel<128><<<grid, 128, 0, st>>>(a);
-  else
-    index_kernel<64><<<grid, 128, 0, st>>>(a);
   ++t_launches;
   return cudaGetLastError();
 }

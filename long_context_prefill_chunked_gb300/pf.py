@@ -177,11 +177,16 @@ def sparse_sizes(q, k, start_pos, block=128) -> SparseSizes:
 @dataclasses.dataclass
 class Selection:
     """Device buffers of a pf_sel: row_bits [B,Hq,C,W] int32 (bit pattern), tile_list
-    [B,Hq,nqt,nblk], tile_cnt [B,Hq,nqt], kbar [B,Hkv,nblk,d] fp32."""
+    [B,Hq,nqt,nblk], tile_cnt [B,Hq,nqt], kbar [2,B,Hkv,nblk,d] fp32 (means, then the
+    library's 16-bit hi/lo split of them)."""
     row_bits: torch.Tensor
     tile_list: torch.Tensor
     tile_cnt: torch.Tensor
     kbar: torch.Tensor
+
+    @property
+    def kbar_mean(self) -> torch.Tensor:
+        return self.kbar[0]
 
     def c_struct(self) -> Sel:
         return Sel(self.row_bits.data_ptr(), self.tile_list.data_ptr(), self.tile_cnt.data_ptr(),
@@ -196,7 +201,7 @@ def alloc_selection(q, k, start_pos, block=128) -> Selection:
     return Selection(torch.empty((B, Hq, C, z.words), dtype=torch.int32, device=dev),
                      torch.empty((B, Hq, z.nqt, z.nblk), dtype=torch.int32, device=dev),
                      torch.empty((B, Hq, z.nqt), dtype=torch.int32, device=dev),
-                     torch.empty((B, Hkv, z.nblk, d), dtype=torch.float32, device=dev))
+                     torch.empty((2, B, Hkv, z.nblk, d), dtype=torch.float32, device=dev))
 
 
 def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stream=None) -> Selection:
@@ -241,7 +246,8 @@ def vbar_view(pooled: torch.Tensor, q, k, start_pos, block=128) -> torch.Tensor:
     """The fp32 block means of v at the head of the sparse workspace, [B, Hkv, nblk, d]."""
     z = sparse_sizes(q, k, start_pos, block)
     B, Hkv, d = q.shape[0], k.shape[2], q.shape[3]
-    return pooled[: z.kbar_elems * 4].view(torch.float32).view(B, Hkv, z.nblk, d)
+    n = z.kbar_elems // 2  # pooled elements (kbar_elems also counts the 16-bit split)
+    return pooled[: n * 4].view(torch.float32).view(B, Hkv, z.nblk, d)
 
 
 def stream_status(stream=None):

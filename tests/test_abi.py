@@ -100,8 +100,8 @@ def test_sparse_sizes(lib):
     assert (z.nblk, z.nqt, z.words) == (96, 32, 3)
     assert z.row_bits_elems == 32 * 4096 * 3
     assert z.tile_list_elems == 32 * 32 * 96
-    assert z.kbar_elems == 8 * 96 * 128
-    assert z.pooled_bytes >= z.kbar_elems * (4 + 2 + 2)
+    assert z.kbar_elems == 2 * 8 * 96 * 128
+    assert z.pooled_bytes >= z.kbar_elems // 2 * (4 + 2 + 2)
 
 
 def test_header_cites_the_pages():

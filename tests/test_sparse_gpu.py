@@ -89,7 +89,7 @@ def test_small_planted_selection_and_output(small, s, C):
     check_selection(sel, osel, np.arange(C))
     check_tile_lists(sel, osel, C)
     # pooled keys and values are the fp32 block means
-    kb = sel.kbar.cpu().double().numpy()
+    kb = sel.kbar_mean.cpu().double().numpy()
     assert np.max(np.abs(kb - osel.kbar)) <= 1e-5
     vb = pfx.vbar_view(pooled, q, k, s).cpu().double().numpy()
     assert np.max(np.abs(vb - oracle.pool_blocks(w.f64(w.v[:, :s + C]), 128))) <= 1e-5
