@@ -46,6 +46,17 @@ def flops_equiv(C, s, Hq=HQ, d=D):
     return 4.0 * Hq * d * pairs_causal(C, s)
 
 
+def kernel_source_hash():
+    """sha256 over the sources that define the dense attention kernel (a stored ncu traffic
+    figure is only reported while it still matches)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "kernels.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "long_context_prefill_chunked_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
         os.environ.get("LOCAL_RANK", "0"))
@@ -181,12 +192,14 @@ def run_case(args):
     import prefill_inputs as pi
     w = pi.config(4)
     to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
-    s = N_TOK - CHUNK
+    s = args.start
+    if s % CHUNK != 0 or not 0 <= s < N_TOK:
+        raise SystemExit("--start must be a multiple of %d below %d" % (CHUNK, N_TOK))
     K, V = to_dev(w.k), to_dev(w.v)
-    Q = to_dev(w.q[:, s:]) if args.case == "dense-chunk" else to_dev(w.q)
+    Q = to_dev(w.q[:, s:s + CHUNK]) if args.case == "dense-chunk" else to_dev(w.q)
     if args.case == "dense-chunk":
         out = torch.empty((1, CHUNK, HQ, D), dtype=torch.float32, device="cuda")
-        run = lambda: pfx.attn_dense(Q, K[:, :s], V[:, :s], K[:, s:], V[:, s:], s, out=out)
+        run = lambda: pfx.attn_dense(Q, K[:, :s], V[:, :s], K[:, s:s + CHUNK], V[:, s:s + CHUNK], s, out=out)
         flops = flops_equiv(CHUNK, s)
     else:
         sel = pfx.alloc_selection(Q, K, 0)
@@ -209,7 +222,8 @@ def run_case(args):
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))
     pfx.stream_status()
-    print(json.dumps({"case": args.case, "ms": times, "tflops_equiv": flops / (min(times) * 1e-3) / 1e12}))
+    print(json.dumps({"case": args.case, "start": s if args.case == "dense-chunk" else 0, "ms": times,
+                      "tflops_equiv": flops / (min(times) * 1e-3) / 1e12}))
     return 0
 
 
@@ -225,7 +239,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse"],
                     help="dense-chunk / sparse: a small profiling case (one 4096-row chunk at "
-                         "start 28672, or the 32K block-sparse pair), timings only")
+                         "--start, or the 32K block-sparse pair), timings only")
+    ap.add_argument("--start", type=int, default=N_TOK - CHUNK,
+                    help="dense-chunk case: the chunk's first token (a multiple of 4096)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -329,10 +345,14 @@ def main():
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = f_dense / (d_ms * 1e-3) / 1e12
-    traffic = None
+    traffic, traffic_note = None, "no ncu capture on file"
     tpath = os.path.join(ROOT, "profiles", "attn_dense_traffic.json")
     if os.path.exists(tpath):
-        traffic = json.load(open(tpath)).get("bytes_per_launch")
+        tj = json.load(open(tpath))
+        if tj.get("source_sha256") == kernel_source_hash():
+            traffic, traffic_note = tj.get("bytes_per_launch"), tj.get("note")
+        else:
+            traffic_note = "kernel source changed since the ncu capture"
 
     tc = sel.tile_cnt.cpu().numpy().astype(np.float64)
     n_qt = tc.shape[-1]
@@ -348,10 +368,8 @@ def main():
     hck = torch.empty(cache_k.shape, dtype=cache_k.dtype).pin_memory()
     hcv = torch.empty(cache_v.shape, dtype=cache_v.dtype).pin_memory()
     dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    e0, e1 = mk(), mk()
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
+
+    def e2e_step():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
@@ -360,6 +378,13 @@ def main():
         ho_s.copy_(out_s, non_blocking=True)
         hck.copy_(cache_k, non_blocking=True)
         hcv.copy_(cache_v, non_blocking=True)
+
+    e2e_step()                              # untimed warm-up of the copy path
+    e0, e1 = mk(), mk()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
@@ -392,7 +417,7 @@ def main():
                              "skip_share_tiles": skip_tiles},
         },
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "traffic": traffic, "traffic_note": traffic_note,
                      "kernel": "attn_fwd_kernel<causal> (8 launches per step; window includes the "
                                "chunk's two cache-layout copies)",
                      "peak_source": "%s bf16_tflops (burst)" % peak_src},

@@ -63,7 +63,6 @@ struct PoolArgs {
   void* out_lo;          // [B, H, nblk, d] 16-bit round of (mean - hi), may be null
 };
 cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st);
-cudaError_t launch_f32_to_lp(const float* src, void* dst, long long n, int bf16, cudaStream_t st);
 
 struct IndexArgs {
   int ab_type;           // 0 = f16, 1 = bf16 (q and the kbar hi/lo split)

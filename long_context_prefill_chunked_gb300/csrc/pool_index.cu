@@ -85,30 +85,11 @@ __global__ void pool_kernel(PoolArgs a, int bf16) {
   }
 }
 
-__global__ void f32_to_lp_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
-                                 long long n, int bf16) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; 2 * i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const float2 v = reinterpret_cast<const float2*>(src)[i];
-    reinterpret_cast<uint32_t*>(dst)[i] = bf16 ? pack_bf16(v.x, v.y) : pack_f16(v.x, v.y);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st) {
   dim3 grid(a.nblk, a.B);
   pool_kernel<<<grid, a.H * a.d / 8, 0, st>>>(a, bf16);
-  ++t_launches;
-  return cudaGetLastError();
-}
-
-cudaError_t launch_f32_to_lp(const float* src, void* dst, long long n, int bf16, cudaStream_t st) {
-  const long long pairs = n / 2;
-  const int threads = 256;
-  long long want = (pairs + threads - 1) / threads;
-  const int grid = (int)(want < 152 * 8 ? (want > 0 ? want : 1) : 152 * 8);
-  f32_to_lp_kernel<<<grid, threads, 0, st>>>(src, static_cast<uint16_t*>(dst), n, bf16);
   ++t_launches;
   return cudaGetLastError();
 }

@@ -116,6 +116,24 @@ def _bth(t: torch.Tensor):
     return I64x3(t.stride(0), t.stride(1), t.stride(2))
 
 
+def _expect(t, shape, name, device):
+    """Refuse a tensor whose extents differ from what the call will read or write: the C
+    ABI takes bare pointers and cannot check them itself."""
+    if t is None:
+        raise ValueError("%s is required" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def _expect_selection(sel, z, B, C, Hq, Hkv, d, device):
+    _expect(sel.row_bits, (B, Hq, C, z.words), "sel.row_bits", device)
+    _expect(sel.tile_list, (B, Hq, z.nqt, z.nblk), "sel.tile_list", device)
+    _expect(sel.tile_cnt, (B, Hq, z.nqt), "sel.tile_cnt", device)
+    _expect(sel.kbar, (2, B, Hkv, z.nblk, d), "sel.kbar", device)
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -138,9 +156,26 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
                out_v=None, out_dtype=torch.float32, scale=0.0, stream=None):
     """Dense chunked prefill (pf_attn_dense); returns out [B, C, Hq, d]."""
     lib = load()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, C, Hq, d]")
     B, C, Hq, d = q.shape
+    Hkv = k_chunk.shape[2] if k_chunk is not None and k_chunk.dim() == 4 else -1
+    dev = q.device
+    _expect(k_chunk, (B, C, Hkv, d), "k_chunk", dev)
+    _expect(v_chunk, (B, C, Hkv, d), "v_chunk", dev)
+    if start_pos > 0:
+        _expect(k_hist, (B, start_pos, Hkv, d), "k_hist", dev)
+        _expect(v_hist, (B, start_pos, Hkv, d), "v_hist", dev)
     if out is None:
         out = torch.empty((B, C, Hq, d), dtype=out_dtype, device=q.device)
+    _expect(out, (B, C, Hq, d), "out", dev)
+    if (out_k is None) != (out_v is None):
+        raise ValueError("out_k and out_v go together")
+    if out_k is not None:
+        _expect(out_k, (B, Hkv, C, d), "out_k", dev)
+        _expect(out_v, (B, Hkv, C, d), "out_v", dev)
+    if mask is not None:
+        _expect(mask, (C, start_pos + C), "mask", dev)
     sh = make_shape(q, k_chunk, out.dtype, scale)
     sh.kc_stride = _bth(k_chunk)
     if v_chunk.stride() != k_chunk.stride():
@@ -207,8 +242,13 @@ def alloc_selection(q, k, start_pos, block=128) -> Selection:
 def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stream=None) -> Selection:
     """Pooled block selection (pf_block_index)."""
     lib = load()
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, C, Hq, d] and k [B, start_pos + C, Hkv, d]")
+    B, C, Hq, d = q.shape
+    _expect(k, (B, start_pos + C, k.shape[2], d), "k", q.device)
     if sel is None:
         sel = alloc_selection(q, k, start_pos, block)
+    _expect_selection(sel, sparse_sizes(q, k, start_pos, block), B, C, Hq, k.shape[2], d, q.device)
     sh = make_shape(q, k, torch.float32, scale)
     sh.kh_stride = _bth(k)
     cs = sel.c_struct()
@@ -226,11 +266,22 @@ def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=
                 out_dtype=torch.float32, scale=0.0, stream=None):
     """Block-sparse attention with pooled correction (pf_attn_sparse); returns out."""
     lib = load()
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, C, Hq, d] and k, v [B, start_pos + C, Hkv, d]")
     B, C, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dev = q.device
+    _expect(k, (B, start_pos + C, Hkv, d), "k", dev)
+    _expect(v, (B, start_pos + C, Hkv, d), "v", dev)
+    z = sparse_sizes(q, k, start_pos, block)
+    _expect_selection(sel, z, B, C, Hq, Hkv, d, dev)
     if out is None:
         out = torch.empty((B, C, Hq, d), dtype=out_dtype, device=q.device)
+    _expect(out, (B, C, Hq, d), "out", dev)
     if pooled is None:
         pooled = alloc_pooled(q, k, start_pos, block)
+    if pooled.device != dev or pooled.numel() * pooled.element_size() < z.pooled_bytes:
+        raise ValueError("pooled must hold %d bytes on %s" % (z.pooled_bytes, dev))
     if v.stride() != k.stride():
         raise ValueError("k and v must share strides")
     sh = make_shape(q, k, out.dtype, scale)

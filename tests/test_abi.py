@@ -108,3 +108,30 @@ def test_header_cites_the_pages():
     text = open(HEADER).read()
     for page in ("ANE Prefill Research", "Porting FlashPrefill V2 to Apple silicon"):
         assert page in text
+
+
+def test_binding_refuses_mismatched_extents(lib):
+    """The C ABI takes bare pointers; the binding must refuse a buffer whose extents differ from
+    what the call reads or writes (these raise before any library call, so CPU tensors do)."""
+    import torch
+    B, C, Hq, Hkv, d, s = 1, 256, 4, 2, 128, 128
+    bf = torch.bfloat16
+    q = torch.zeros((B, C, Hq, d), dtype=bf)
+    kc = torch.zeros((B, C, Hkv, d), dtype=bf)
+    kh = torch.zeros((B, s, Hkv, d), dtype=bf)
+    with pytest.raises(ValueError, match="out"):            # output with the wrong row count
+        pf.attn_dense(q, kh, kh, kc, kc, s, out=torch.zeros((B, 4 * C, Hq, d)))
+    with pytest.raises(ValueError, match="k_chunk"):        # chunk keys shorter than the queries
+        pf.attn_dense(q, kh, kh, kc[:, :128], kc[:, :128], s)
+    with pytest.raises(ValueError, match="k_hist"):         # history shorter than start_pos
+        pf.attn_dense(q, kh[:, :64], kh[:, :64], kc, kc, s)
+    with pytest.raises(ValueError, match="out_k"):          # cache slice of the wrong length
+        pf.attn_dense(q, kh, kh, kc, kc, s, out=torch.zeros((B, C, Hq, d)),
+                      out_k=torch.zeros((B, Hkv, C // 2, d), dtype=bf),
+                      out_v=torch.zeros((B, Hkv, C // 2, d), dtype=bf))
+    with pytest.raises(ValueError, match="mask"):
+        pf.attn_dense(q, kh, kh, kc, kc, s, out=torch.zeros((B, C, Hq, d)),
+                      mask=torch.zeros((C, C)))
+    k_all = torch.zeros((B, s + C, Hkv, d), dtype=bf)
+    with pytest.raises(ValueError, match="k"):
+        pf.block_index(q, k_all[:, :C], s)
