@@ -100,6 +100,13 @@ typedef struct {
  * out_k / out_v (optional, both or neither): bit copies of k_chunk / v_chunk
  * written at okv_stride, by default head-major [B, Hkv, C, d], so a caller can
  * point them at row start_pos of its own cache.
+ * workspace (optional, device memory owned by the caller, 16-byte aligned,
+ * workspace_bytes >= pf_dense_workspace_bytes, PF_EINVAL otherwise): lets the
+ * call split the key range of its last, partial wave of work units across the
+ * idle SMs; the parts' partial results (O, running max, sum) are merged on the
+ * device with the same softmax identity, so the output matches the unsplit
+ * call up to fp32 rounding order.  NULL runs every unit whole.  Calls that can
+ * overlap on the GPU need separate workspaces.
  * Requirements: start_pos % 128 == 0 (PF_EUNSUPPORTED otherwise); every base
  * pointer 16-byte aligned and every stride a multiple of 16 bytes (PF_EINVAL);
  * k_hist / v_hist may be NULL when start_pos == 0.
@@ -107,7 +114,11 @@ typedef struct {
 pf_status pf_attn_dense(const pf_shape* shape, const void* q, const void* k_hist,
                         const void* v_hist, const void* k_chunk, const void* v_chunk,
                         const void* mask, int32_t start_pos, void* out, void* out_k,
-                        void* out_v, void* stream);
+                        void* out_v, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Bytes of the optional pf_attn_dense workspace for shape->d on the current
+ * device (about 20 MB for d = 128 on 152 SMs; independent of the sequence). */
+pf_status pf_dense_workspace_bytes(const pf_shape* shape, int64_t* bytes);
 
 /* Block selection produced by pf_block_index and consumed by pf_attn_sparse.
  * nblk = ceil((start_pos + C) / block); nqt = ceil(C / 128); W = ceil(nblk / 32). */

@@ -113,6 +113,26 @@ __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&x)[128]) {
   for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive output values of one row, already divided by l, in the output type.
+__device__ __forceinline__ void store_out32(const AttnArgs& a, long long off, const float (&v)[32]) {
+  if (a.out_dtype == 2) {
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = (a.out_dtype == 1) ? pack_bf16(v[8 * i + 2 * e], v[8 * i + 2 * e + 1])
+                                  : pack_f16(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
+      dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnArgs a) {
@@ -126,12 +146,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_BAR + 8 * N_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_BAR + 8 * N_BARS + 4);
   int* n_ex_slot = reinterpret_cast<int*>(smem + SM_BAR + 8 * N_BARS + 8);
+  int* last_part = reinterpret_cast<int*>(smem + SM_BAR + 8 * N_BARS + 12);
   const uint32_t* kept_bm = reinterpret_cast<const uint32_t*>(smem + SM_BM);
 
-  // ---- work unit: heaviest query tiles first (longest causal key range)
+  // ---- work unit: heaviest query tiles first (longest causal key range).  CTAs past
+  // n_whole are the parts of the last (lightest) units, split_k consecutive CTAs per unit.
+  int unit = (int)blockIdx.x, part = 0, split = -1;
+  if (unit >= a.n_whole) {
+    split = (unit - a.n_whole) / a.split_k;
+    part = (unit - a.n_whole) % a.split_k;
+    unit = a.n_whole + split;
+  }
   const int per_qt = a.n_hp * a.B;
-  const int qt = a.n_qt - 1 - (int)blockIdx.x / per_qt;
-  const int rem = (int)blockIdx.x % per_qt;
+  const int qt = a.n_qt - 1 - unit / per_qt;
+  const int rem = unit % per_qt;
   const int b = rem / a.n_hp;
   const int h0 = (rem % a.n_hp) * a.slots;
   const int g = h0 / a.G;
@@ -202,6 +230,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     n_pool = (ob + kTile - 1) / kTile;
     n_tiles = n_pool + *n_ex_slot;
   }
+  // a split unit's part covers key tiles [j0, j0 + n_tiles); loops below count locally from 0
+  int j0 = 0;
+  const bool has_last_tile = split < 0 || part == a.split_k - 1;
+  if (split >= 0) {
+    j0 = part * n_tiles / a.split_k;
+    n_tiles = (part + 1) * n_tiles / a.split_k - j0;
+  }
 
   // 384 threads x 168 registers at launch; the softmax warpgroups take 216,
   // the producer/MMA/converter warpgroup keeps 72: 2*128*216 + 128*72 = 384*168.
@@ -236,7 +271,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           c1 = j * kTile;
           c2 = g;
         } else {
-          const int kt = (MODE == MODE_SPARSE) ? walk.next() : j;
+          const int kt = (MODE == MODE_SPARSE) ? walk.next() : j0 + j;
           if (kt < a.n_hist_tiles) {
             mk = &maps.kh;
             mv = &maps.vh;
@@ -410,14 +445,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ld_row128(t_s, x);
       float xs = a.scale_log2, bias = 0.f;
       if (MODE == MODE_CAUSAL) {
-        if (j == n_tiles - 1) {  // diagonal tile: key q0 + c visible iff c <= r
+        if (j == n_tiles - 1 && has_last_tile) {  // diagonal tile: key q0 + c visible iff c <= r
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > r) x[c] = -INFINITY;
         }
       } else if (MODE == MODE_MASK) {
         xs = 1.f;
-        const int key0 = j * kTile;
+        const int key0 = (j0 + j) * kTile;
         if (valid && a.mask_vec && key0 + kTile <= a.T) {
           if (a.mask_f16) {
             const uint4* mp = reinterpret_cast<const uint4*>(
@@ -560,36 +595,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ---- epilogue: out = O / l
     if (ok)
       ok = wait_all(BAR(B_OF), 0, a.timeout, abort_flag, a.status, (R_SOFT << 8) | B_OF);
-    if (ok) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      const long long obase = (long long)b * a.o_sb + (long long)row * a.o_st + (long long)h * a.o_sh;
-      for (int c0 = 0; c0 < a.d; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c0, o);
-        tmem_wait_ld();
-        if (valid) {
-          if (a.out_dtype == 2) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + obase + c0);
+    const long long obase = (long long)b * a.o_sb + (long long)row * a.o_st + (long long)h * a.o_sh;
+    if (split < 0) {
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        for (int c0 = 0; c0 < a.d; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c0, o);
+          tmem_wait_ld();
+          float v[32];
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                   __uint_as_float(o[4 * v + 2]) * inv,
-                                   __uint_as_float(o[4 * v + 3]) * inv);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + obase + c0);
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv;
+          if (valid) store_out32(a, obase + c0, v);
+        }
+      }
+    } else {
+      // A part of a split unit: O (relative to this part's running max m), m and l go to
+      // the workspace, column-major so that a warp's rows are contiguous; the last part to
+      // finish combines them: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p.
+      const long long pstride = (long long)kTile * (a.d + 2);
+      float* wp = a.ws_part + ((long long)(split * a.split_k + part) * 2 + sl) * pstride;
+      if (ok) {
+        tc_fence_after();
+        for (int c0 = 0; c0 < a.d; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c0, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w[4];
+          for (int i = 0; i < 32; ++i) wp[(long long)(c0 + i) * kTile + r] = __uint_as_float(o[i]);
+        }
+        wp[(long long)a.d * kTile + r] = m;
+        wp[(long long)(a.d + 1) * kTile + r] = l;
+      }
+      __threadfence();
+      named_bar_sync(1, 128u * (uint32_t)a.slots);
+      if (threadIdx.x == 0)
+        *last_part = (!*abort_flag && atomicAdd(a.ws_cnt + split, 1) == a.split_k - 1) ? 1 : 0;
+      named_bar_sync(1, 128u * (uint32_t)a.slots);
+      if (*last_part) {
+        __threadfence();
+        const float* p0 = a.ws_part + ((long long)split * a.split_k * 2 + sl) * pstride;
+        float M = -INFINITY;
+        for (int p = 0; p < a.split_k; ++p)
+          M = fmaxf(M, __ldcg(p0 + p * 2 * pstride + (long long)a.d * kTile + r));
+        float wgt[kMaxSplit], L = 0.f;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float lo = __uint_as_float(o[8 * v + 2 * e]) * inv;
-                const float hi = __uint_as_float(o[8 * v + 2 * e + 1]) * inv;
-                w[e] = (a.out_dtype == 1) ? pack_bf16(lo, hi) : pack_f16(lo, hi);
-              }
-              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int p = 0; p < kMaxSplit; ++p) {
+          wgt[p] = 0.f;
+          if (p < a.split_k) {
+            const float mp = __ldcg(p0 + p * 2 * pstride + (long long)a.d * kTile + r);
+            wgt[p] = (mp == -INFINITY) ? 0.f : ex2(mp - M);
+            L += wgt[p] * __ldcg(p0 + p * 2 * pstride + (long long)(a.d + 1) * kTile + r);
+          }
+        }
+        const float inv = 1.f / L;
+        for (int c0 = 0; c0 < a.d; c0 += 32) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll
+          for (int p = 0; p < kMaxSplit; ++p) {
+            if (p < a.split_k) {
+              const float* op = p0 + p * 2 * pstride + (long long)c0 * kTile + r;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = fmaf(wgt[p], __ldcg(op + (long long)i * kTile), v[i]);
             }
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= inv;
+          if (valid) store_out32(a, obase + c0, v);
         }
       }
     }
@@ -629,7 +704,8 @@ cudaError_t launch_mode(const AttnMaps& maps, const AttnArgs& a, cudaStream_t st
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int grid = a.n_qt * a.n_hp * a.B;
+  const int units = a.n_qt * a.n_hp * a.B;
+  const int grid = a.n_whole + (units - a.n_whole) * a.split_k;
   attn_fwd_kernel<MODE><<<grid, kAttnThreads, SM_ALLOC, st>>>(maps, a);
   ++t_launches;
   return cudaGetLastError();

@@ -7,6 +7,7 @@
 namespace pf {
 
 constexpr int kTile = 128;        // query rows and keys per tile (= key block of the sparse path)
+constexpr int kMaxSplit = 8;      // parts of one split dense unit (tail split)
 constexpr int kAttnThreads = 384; // 8 softmax warps (2 slots x 4), TMA warp, MMA warp, 2 V converters
 
 enum AttnMode : int { MODE_CAUSAL = 0, MODE_MASK = 1, MODE_SPARSE = 2 };
@@ -35,6 +36,13 @@ struct AttnArgs {
   const int32_t* tile_cnt;    // [B, Hq, n_qt]
   int words, nblk;
   float log2_nb;              // log2 of the pooled weight n_b (block size)
+  // tail split (MODE_CAUSAL / MODE_MASK): units [0, n_whole) run whole, one CTA each; every
+  // later unit runs as split_k CTAs over consecutive key-tile ranges, and the last of them to
+  // finish merges the parts' partial results
+  int n_whole;          // = number of units when nothing is split
+  int split_k;          // parts per split unit (1 = no split)
+  float* ws_part;       // per part and slot: O^T [d][128] then m [128] and l [128], fp32
+  int* ws_cnt;          // finished parts per split unit, zero at launch
   // robustness
   unsigned* status;     // device status words (timeout flag, where)
   long long timeout;    // bounded-wait limit, SM cycles

@@ -163,6 +163,49 @@ void fill_attn_common(const pf_shape* sh, int32_t start_pos, AttnArgs& a) {
   a.timeout = g_timeout;
   a.withhold = g_withhold;
   a.status = status_words();
+  a.n_whole = a.n_qt * a.n_hp * a.B;  // no tail split unless a dense call plans one
+  a.split_k = 1;
+}
+
+// SMs of the current device (cached per device).
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+constexpr int kMinPartTiles = 4;      // a part gets at least this many key tiles
+constexpr long long kCountBytes = 4096;  // counter area at the head of the workspace
+
+long long dense_workspace_bytes(int d, int sms) {
+  return kCountBytes + (long long)sms * 2 * kTile * (d + 2) * 4;
+}
+
+// Tail split.  With U units and P SMs, the last wave holds W = U mod P units (all U when
+// U < P) on P SMs; each of those units (the lightest, since units run heaviest first) is
+// cut into k = P / W parts of consecutive key tiles so that the last wave fills the GPU.
+// Needs W * k * 2 * 128 * (d + 2) floats of partials, at most P parts.
+void plan_split(AttnArgs& a, int mode, void* ws) {
+  const int P = sm_count();
+  const int U = a.n_qt * a.n_hp * a.B;
+  if (P <= 0 || ws == nullptr) return;
+  const int W = (U < P) ? U : U % P;
+  if (W == 0 || W > (int)(kCountBytes / 4)) return;
+  const int min_tiles = (mode == MODE_CAUSAL) ? a.s / kTile + 1 : (a.T + kTile - 1) / kTile;
+  int k = P / W;
+  if (k > kMaxSplit) k = kMaxSplit;
+  if (k > min_tiles / kMinPartTiles) k = min_tiles / kMinPartTiles;
+  if (k < 2) return;
+  a.n_whole = U - W;
+  a.split_k = k;
+  a.ws_cnt = static_cast<int*>(ws);
+  a.ws_part = reinterpret_cast<float*>(static_cast<char*>(ws) + kCountBytes);
 }
 
 }  // namespace
@@ -199,9 +242,19 @@ pf_status pf_stream_status(void* stream) {
               w[1] >> 8, w[1] & 0xFFu);
 }
 
+pf_status pf_dense_workspace_bytes(const pf_shape* sh, int64_t* bytes) {
+  if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
+  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  const int P = sm_count();
+  if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
+  *bytes = dense_workspace_bytes(sh->d, P);
+  return PF_OK;
+}
+
 pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, const void* v_hist,
                         const void* k_chunk, const void* v_chunk, const void* mask,
-                        int32_t start_pos, void* out, void* out_k, void* out_v, void* stream) {
+                        int32_t start_pos, void* out, void* out_k, void* out_v, void* workspace,
+                        int64_t workspace_bytes, void* stream) {
   pf_status rc = check_common(sh, start_pos);
   if (rc != PF_OK) return rc;
   if (q == nullptr || k_chunk == nullptr || v_chunk == nullptr || out == nullptr)
@@ -211,7 +264,14 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
   if ((out_k == nullptr) != (out_v == nullptr)) return fail(PF_EINVAL, "give both out_k and out_v, or neither");
   if (mask != nullptr && sh->mask_dtype != PF_F32 && sh->mask_dtype != PF_F16)
     return fail(PF_EUNSUPPORTED, "mask dtype must be f32 or f16 (bf16 cannot hold -30000 exactly)");
-  const void* ptrs[] = {q, k_hist, v_hist, k_chunk, v_chunk, out, out_k, out_v};
+  if (workspace != nullptr) {
+    const int P = sm_count();
+    if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
+    if (workspace_bytes < dense_workspace_bytes(sh->d, P))
+      return fail(PF_EINVAL, "workspace of %lld bytes is smaller than pf_dense_workspace_bytes (%lld)",
+                  (long long)workspace_bytes, dense_workspace_bytes(sh->d, P));
+  }
+  const void* ptrs[] = {q, k_hist, v_hist, k_chunk, v_chunk, out, out_k, out_v, workspace};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return fail(PF_EINVAL, "every base pointer must be 16-byte aligned");
   const int B = sh->B, C = sh->C, Hq = sh->Hq, Hkv = sh->Hkv, d = sh->d, s = start_pos;
@@ -266,7 +326,14 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
 
   if (a.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_attn(maps, a, mode, st);
+  cudaError_t e;
+  plan_split(a, mode, workspace);
+  if (a.split_k > 1) {
+    const int n_split = a.n_qt * a.n_hp * a.B - a.n_whole;
+    if ((e = cudaMemsetAsync(a.ws_cnt, 0, sizeof(int) * n_split, st)) != cudaSuccess)
+      return cuda_fail(e, "workspace counters");
+  }
+  e = launch_attn(maps, a, mode, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (out_k != nullptr) {
     if ((e = launch_kv_relayout(k_chunk, out_k, B, C, Hkv, d, kcs, okv, st)) != cudaSuccess)

@@ -77,6 +77,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   }
 }
 
+// Barrier over a subset of the CTA's warps (id 1..15; every participating thread
+// executes it; n is a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Register rebalancing between warpgroups (all four warps of a warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {

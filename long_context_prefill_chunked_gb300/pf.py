@@ -27,7 +27,8 @@ PF_F16, PF_BF16, PF_F32 = range(3)
 STATUS_NAMES = {0: "PF_OK", 1: "PF_EINVAL", 2: "PF_EUNSUPPORTED", 3: "PF_ECUDA", 4: "PF_ETIMEOUT",
                 5: "PF_ERANGE"}
 
-EXPORTS = ["pf_attn_dense", "pf_block_index", "pf_attn_sparse", "pf_sparse_query_sizes",
+EXPORTS = ["pf_attn_dense", "pf_dense_workspace_bytes", "pf_block_index", "pf_attn_sparse",
+           "pf_sparse_query_sizes",
            "pf_stream_status", "pf_set_wait_timeout", "pf_set_debug_withhold", "pf_launch_count",
            "pf_last_error", "pf_version"]
 
@@ -71,7 +72,8 @@ def load() -> ctypes.CDLL:
         raise ImportError("libpf.so not found at %s: run __graft_entry__.build() first" % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     V, I32, I64, F, P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.POINTER
-    lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V]
+    lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V, I64, V]
+    lib.pf_dense_workspace_bytes.argtypes = [P(Shape), P(I64)]
     lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(Sel), V]
     lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V]
     lib.pf_sparse_query_sizes.argtypes = [P(Shape), I32, I32, P(SparseSizes)]
@@ -84,8 +86,8 @@ def load() -> ctypes.CDLL:
     lib.pf_launch_count.restype = I64
     lib.pf_last_error.restype = ctypes.c_char_p
     lib.pf_version.restype = ctypes.c_char_p
-    for name in ("pf_attn_dense", "pf_block_index", "pf_attn_sparse", "pf_sparse_query_sizes",
-                 "pf_stream_status"):
+    for name in ("pf_attn_dense", "pf_dense_workspace_bytes", "pf_block_index", "pf_attn_sparse",
+                 "pf_sparse_query_sizes", "pf_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -152,9 +154,31 @@ def make_shape(q, k_like, out_dtype, scale=0.0) -> Shape:
     return sh
 
 
+_WORKSPACES = {}
+
+
+def dense_workspace(q, stream=None) -> torch.Tensor:
+    """The pf_attn_dense tail-split workspace for q's head dim, one per (device, stream) so
+    that calls on different streams never share one."""
+    lib = load()
+    sh = Shape()
+    sh.d = q.shape[-1]
+    n = ctypes.c_int64(0)
+    with torch.cuda.device(q.device):
+        _check(lib.pf_dense_workspace_bytes(ctypes.byref(sh), ctypes.byref(n)))
+    key = (q.device, _stream(stream).value, int(n.value))
+    ws = _WORKSPACES.get(key)
+    if ws is None:
+        ws = torch.empty((int(n.value),), dtype=torch.uint8, device=q.device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=None, out_k=None,
-               out_v=None, out_dtype=torch.float32, scale=0.0, stream=None):
-    """Dense chunked prefill (pf_attn_dense); returns out [B, C, Hq, d]."""
+               out_v=None, out_dtype=torch.float32, scale=0.0, stream=None, workspace=True):
+    """Dense chunked prefill (pf_attn_dense); returns out [B, C, Hq, d].  workspace: True
+    uses a cached per-(device, stream) buffer (tail split on), None runs every unit whole,
+    or a caller-owned uint8 tensor of at least pf_dense_workspace_bytes."""
     lib = load()
     if q.dim() != 4:
         raise ValueError("q must be [B, C, Hq, d]")
@@ -176,6 +200,13 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
         _expect(out_v, (B, Hkv, C, d), "out_v", dev)
     if mask is not None:
         _expect(mask, (C, start_pos + C), "mask", dev)
+    if workspace is True:
+        workspace = dense_workspace(q, stream)
+    elif workspace is False:
+        workspace = None
+    if workspace is not None and workspace.device != dev:
+        raise ValueError("workspace is on %s, expected %s" % (workspace.device, dev))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     sh = make_shape(q, k_chunk, out.dtype, scale)
     sh.kc_stride = _bth(k_chunk)
     if v_chunk.stride() != k_chunk.stride():
@@ -197,7 +228,7 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
     _check(lib.pf_attn_dense(ctypes.byref(sh), _ptr(q), _ptr(k_hist if start_pos > 0 else None),
                              _ptr(v_hist if start_pos > 0 else None), _ptr(k_chunk), _ptr(v_chunk),
                              _ptr(mask), int(start_pos), _ptr(out), _ptr(out_k), _ptr(out_v),
-                             _stream(stream)))
+                             _ptr(workspace), int(ws_bytes), _stream(stream)))
     return out
 
 

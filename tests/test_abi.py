@@ -50,9 +50,10 @@ FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: validation fails fir
 MISALIGNED = ctypes.c_void_p(0x100008)
 
 
-def dense(lib, sh, q=FAKE, kh=None, vh=None, kc=FAKE, vc=FAKE, mask=None, s=0, out=FAKE, ok=None, ov=None):
+def dense(lib, sh, q=FAKE, kh=None, vh=None, kc=FAKE, vc=FAKE, mask=None, s=0, out=FAKE, ok=None, ov=None,
+          ws=None, ws_bytes=0):
     return lib.pf_attn_dense(ctypes.byref(sh) if sh is not None else None, q, kh, vh, kc, vc, mask, s,
-                             out, ok, ov, None)
+                             out, ok, ov, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -172,3 +172,43 @@ def test_value_outside_fp16_range_is_reported():
     vc[0, 17, 1, 5] = 1.0
     pfx.attn_dense(q, kh, vh, kc, vc, 0)
     pfx.stream_status()
+
+
+# --------------------------------------------------------------------------- tail split
+@pytest.mark.parametrize("case", ["causal", "mask", "ragged", "bf16-out"])
+def test_tail_split_matches_oracle_and_unsplit(case):
+    """32 units (8 query tiles x 4 head pairs) on a 152-SM GPU: with a workspace every unit's
+    key range is cut into parts whose partial (O, m, l) are merged on the device; the result
+    must meet the oracle like the unsplit call does."""
+    C = 1000 if case == "ragged" else 1024
+    w = pi.normal_workload("split-" + case, 61, 1, 8, 2, 128, 2048 + C, C, "bf16")
+    s = 2048
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(s))
+    mask = None
+    if case == "mask":
+        g = np.random.default_rng(62)
+        mask = np.zeros((C, s + C), dtype=np.float32)
+        mask[g.random(mask.shape) < 0.3] = -30000.0
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    odt = torch.bfloat16 if case == "bf16-out" else torch.float32
+    split = pfx.attn_dense(q, kh, vh, kc, vc, s, mask=dmask, out_dtype=odt, workspace=True)
+    whole = pfx.attn_dense(q, kh, vh, kc, vc, s, mask=dmask, out_dtype=odt, workspace=None)
+    pfx.stream_status()
+    ref = ref_chunk(w, s, mask)
+    if case == "bf16-out":
+        for out in (split, whole):
+            mx, _ = errors(out, ref)
+            assert mx <= 5e-3 + 2 ** -8 * np.abs(ref).max()
+    else:
+        assert_close(split, ref, "split " + case)
+        assert_close(whole, ref, "whole " + case)
+    mx, _ = errors(split, whole.double().cpu().numpy())
+    assert mx <= 2e-3
+
+
+def test_tail_split_workspace_too_small_is_refused():
+    w = pi.normal_workload("split-small-ws", 63, 1, 8, 2, 128, 1024, 512, "bf16")
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(512))
+    with pytest.raises(pfx.PFError) as e:
+        pfx.attn_dense(q, kh, vh, kc, vc, 512, workspace=torch.empty(1024, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == pf.PF_EINVAL
