@@ -57,6 +57,22 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
+def max_over_ranks(value_ms, device, world):
+    """The slowest rank's time: every rank contributes its own, all receive the maximum."""
+    if world <= 1:
+        return value_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_rank, ms_per_step, world):
+    """Whole-job throughput: every rank processed flops_per_rank in the slowest rank's time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
         os.environ.get("LOCAL_RANK", "0"))
@@ -328,16 +344,12 @@ def main():
     dense_ms = [[a.elapsed_time(b) for a, b in e["dense"]] for e in evs]
     index_ms = [e["index"][0].elapsed_time(e["index"][1]) for e in evs]
     sparse_ms = [e["sparse"][0].elapsed_time(e["sparse"][1]) for e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev, world)
     ms_step = total_ms / args.steps
 
     f_dense = sum(flops_equiv(CHUNK, s) for s in starts)
     f_sparse = flops_equiv(N_TOK, 0)
-    value = world * (f_dense + f_sparse) / (ms_step * 1e-3) / 1e12
+    value = weak_scaling_value(f_dense + f_sparse, ms_step, world)
     tokens_per_s = world * 2 * N_TOK / (ms_step * 1e-3)
 
     # dominant kernel: the dense attention launches (8 per step)
@@ -387,11 +399,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev, world)
     pfx.stream_status(stream)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = sum(x.numel() * x.element_size() for x in (ho_d, ho_s, hck, hcv))
@@ -421,7 +429,7 @@ def main():
                      "kernel": "attn_fwd_kernel<causal> (8 launches per step; window includes the "
                                "chunk's two cache-layout copies)",
                      "peak_source": "%s bf16_tflops (burst)" % peak_src},
-        "e2e": {"value": world * (f_dense + f_sparse) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": weak_scaling_value(f_dense + f_sparse, e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,
