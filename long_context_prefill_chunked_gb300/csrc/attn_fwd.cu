@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float x[128];
       ld_row128(t_s, x);
       float xs = a.scale_log2, bias = 0.f;
+      bool row_skip = false;  // sparse: this row did not keep the tile's block
       if (MODE == MODE_CAUSAL) {
         if (j == n_tiles - 1 && has_last_tile) {  // diagonal tile: key q0 + c visible iff c <= r
 #pragma unroll
@@ -534,12 +535,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int c = 0; c < 128; ++c)
               if (c > r) x[c] = -INFINITY;
           } else {
-            const bool keep =
-                bits_row == nullptr || ((__ldg(bits_row + (kb >> 5)) >> (kb & 31)) & 1u);
-            if (!keep) {
-#pragma unroll
-              for (int c = 0; c < 128; ++c) x[c] = -INFINITY;
-            }
+            // a row that did not keep the block gets P = 0 and leaves its max alone
+            // (row max and offset -inf below) instead of masking 128 scores
+            row_skip = bits_row != nullptr && !((__ldg(bits_row + (kb >> 5)) >> (kb & 31)) & 1u);
           }
         }
       }
@@ -552,7 +550,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mx2 = fmaxf(mx2, x[c + 2]);
         mx3 = fmaxf(mx3, x[c + 3]);
       }
-      const float mraw = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float mraw = row_skip ? -INFINITY : fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       const float mt = (mraw == -INFINITY) ? -INFINITY : fmaf(mraw, xs, bias);
       const bool need = mt > m + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
@@ -571,7 +569,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         m = mn;
       }
-      const float off = bias - ((m == -INFINITY) ? 0.f : m);
+      const float off = row_skip ? -INFINITY : bias - ((m == -INFINITY) ? 0.f : m);
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -596,7 +594,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (ok)
       ok = wait_all(BAR(B_OF), 0, a.timeout, abort_flag, a.status, (R_SOFT << 8) | B_OF);
     const long long obase = (long long)b * a.o_sb + (long long)row * a.o_st + (long long)h * a.o_sh;
-    if (split < 0) {
+    if (split < 0 && MODE == MODE_SPARSE) {
+      // Sparse units are short (tens of tiles): direct row stores keep this mode's loop
+      // registers (a staged tile store measured slower here).
       if (ok) {
         tc_fence_after();
         const float inv = 1.f / l;
@@ -609,6 +609,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv;
           if (valid) store_out32(a, obase + c0, v);
         }
+      }
+    } else if (split < 0) {
+      // Rows are staged in shared memory (the Q and K stages are free once every MMA is
+      // done: slot s uses [64 KB * s, 64 KB * (s + 1))) as 128-byte boxes, 16-byte chunks
+      // swizzled the way the tile store reads them, then one thread per head stores the
+      // head's tile; rows at or past C are dropped by the store.
+      const int es = (a.out_dtype == 2) ? 4 : 2;
+      const int box_cols = 128 / es;  // 32 fp32 or 64 16-bit values per 128-byte box row
+      const int nbox = a.d / box_cols;
+      uint8_t* stage = smem + SM_Q + 65536u * sl;
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        for (int bx = 0; bx < nbox; ++bx) {
+          uint32_t wv[32];
+          if (es == 4) {
+            uint32_t o[32];
+            tmem_ld32(t_o + 32u * bx, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) wv[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
+          } else {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint32_t o[32];
+              tmem_ld32(t_o + 64u * bx + 32u * half, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float lo = __uint_as_float(o[2 * i]) * inv, hi = __uint_as_float(o[2 * i + 1]) * inv;
+                wv[16 * half + i] = (a.out_dtype == 1) ? pack_bf16(lo, hi) : pack_f16(lo, hi);
+              }
+            }
+          }
+          uint4* rowp = reinterpret_cast<uint4*>(stage + 16384u * bx + 128u * r);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            rowp[c ^ (r & 7)] = make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
+        }
+      }
+      fence_proxy_async();  // generic-proxy writes -> visible to the tile store
+      named_bar_sync(2u + (uint32_t)sl, 128u);
+      if (r == 0 && ok) {
+        const uint32_t stage_s = sb + SM_Q + 65536u * sl;
+        for (int bx = 0; bx < nbox; ++bx) tma_store_4d(&maps.out, stage_s + 16384u * bx, bx * box_cols, h, q0, b);
+        bulk_commit();
+        bulk_wait_all();
       }
     } else {
       // A part of a split unit: O (relative to this part's running max m), m and l go to

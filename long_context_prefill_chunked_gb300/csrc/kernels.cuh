@@ -51,6 +51,7 @@ struct AttnArgs {
 
 struct AttnMaps {
   CUtensorMap q, kh, kc, vh, vc, kbar, vbar;
+  CUtensorMap out;  // [B, C, Hq, d] in the output type, box 128 bytes x 1 head x 128 rows
 };
 
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaStream_t st);

@@ -118,6 +118,27 @@ pf_status make_map(CUtensorMap* m, const void* base, pf_dtype dt, uint64_t d0, u
   return PF_OK;
 }
 
+// The output [B, C, Hq, d] (f32, bf16 or f16) for tile stores: dims (d, Hq, C, B), box
+// 128 bytes of d x 1 head x 128 rows, 128-byte swizzle (the kernel stages rows swizzled).
+pf_status map_out(CUtensorMap* m, void* base, pf_dtype dt, int B, int C, int Hq, int d,
+                  const long long s[3]) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(PF_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+  const int es = dt == PF_F32 ? 4 : 2;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)C, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)s[2] * es, (cuuint64_t)s[1] * es, (cuuint64_t)s[0] * es};
+  const cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t = dt == PF_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : dt == PF_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(m, t, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PF_ECUDA, "tensor map for out rejected (CUresult %d)", (int)r);
+  return PF_OK;
+}
+
 // Token-major tensor [B, T, H, d] -> map dims (d, H, T, B), box 64 x 1 x 128.
 pf_status map_tokens(CUtensorMap* m, const void* base, pf_dtype dt, int B, int T, int H, int d,
                      const long long s[3], const char* what) {
@@ -323,6 +344,7 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
   }
   maps.kbar = maps.kc;
   maps.vbar = maps.vc;
+  if ((rc = map_out(&maps.out, out, sh->out_dtype, B, C, Hq, d, os)) != PF_OK) return rc;
 
   if (a.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -526,6 +548,7 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
     return rc;
   maps.kc = maps.kh;
   maps.vc = maps.vh;
+  if ((rc = map_out(&maps.out, out, sh->out_dtype, B, C, Hq, d, os)) != PF_OK) return rc;
   if (a.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
   if ((e = launch_attn(maps, a, MODE_SPARSE, st)) != cudaSuccess) return cuda_fail(e, "attention launch");
   return PF_OK;
