@@ -206,8 +206,21 @@ def run_case(args):
     __graft_entry__.build()
     import long_context_prefill_chunked_gb300 as pfx
     import prefill_inputs as pi
-    w = pi.config(4)
+    w = pi.config(5 if args.case == "sparse-128k-chunk" else 4)
     to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    if args.case == "sparse-128k-chunk":
+        # the last 4096-row chunk of the 128K planted prompt: selection and block-sparse
+        # attention against a 131072-key history (K/V 268 MB each, beyond L2)
+        s = w.N - CHUNK
+        K, V, Q = to_dev(w.k), to_dev(w.v), to_dev(w.q[:, s:])
+        sel = pfx.alloc_selection(Q, K, s)
+        pooled = pfx.alloc_pooled(Q, K, s)
+        out = torch.empty((1, CHUNK, HQ, D), dtype=torch.float32, device="cuda")
+
+        def run():
+            pfx.block_index(Q, K, s, BLOCK, ALPHA, sel=sel)
+            pfx.attn_sparse(Q, K, V, s, sel, pooled=pooled, out=out)
+        return _time_case(args, pfx, run, flops_equiv(CHUNK, s), s)
     s = args.start
     if s % CHUNK != 0 or not 0 <= s < N_TOK:
         raise SystemExit("--start must be a multiple of %d below %d" % (CHUNK, N_TOK))
@@ -226,6 +239,11 @@ def run_case(args):
             pfx.block_index(Q, K, 0, BLOCK, ALPHA, sel=sel)
             pfx.attn_sparse(Q, K, V, 0, sel, pooled=pooled, out=out)
         flops = flops_equiv(N_TOK, 0)
+    return _time_case(args, pfx, run, flops, s if args.case == "dense-chunk" else 0)
+
+
+def _time_case(args, pfx, run, flops, start):
+    import torch
     for _ in range(args.warmup):
         run()
     pfx.stream_status()
@@ -238,7 +256,7 @@ def run_case(args):
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))
     pfx.stream_status()
-    print(json.dumps({"case": args.case, "start": s if args.case == "dense-chunk" else 0, "ms": times,
+    print(json.dumps({"case": args.case, "start": start, "ms": times,
                       "tflops_equiv": flops / (min(times) * 1e-3) / 1e12}))
     return 0
 
@@ -253,9 +271,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse"],
-                    help="dense-chunk / sparse: a small profiling case (one 4096-row chunk at "
-                         "--start, or the 32K block-sparse pair), timings only")
+    ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse", "sparse-128k-chunk"],
+                    help="profiling cases, timings only: dense-chunk (one 4096-row chunk at "
+                         "--start), sparse (the 32K block-sparse pair), sparse-128k-chunk (the "
+                         "pair for the last 4096-row chunk of the 128K prompt)")
     ap.add_argument("--start", type=int, default=N_TOK - CHUNK,
                     help="dense-chunk case: the chunk's first token (a multiple of 4096)")
     args = ap.parse_args()

@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   // ---- work unit: heaviest query tiles first (longest causal key range).  CTAs past
   // n_whole are the parts of the last (lightest) units, split_k consecutive CTAs per unit.
-  int unit = (int)blockIdx.x, part = 0, split = -1;
+  int unit = (MODE == MODE_SPARSE && a.perm != nullptr) ? __ldg(a.perm + blockIdx.x) : (int)blockIdx.x;
+  int part = 0, split = -1;
   if (unit >= a.n_whole) {
     split = (unit - a.n_whole) / a.split_k;
     part = (unit - a.n_whole) % a.split_k;

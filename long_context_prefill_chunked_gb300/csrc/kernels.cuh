@@ -39,6 +39,7 @@ struct AttnArgs {
   // tail split (MODE_CAUSAL / MODE_MASK): units [0, n_whole) run whole, one CTA each; every
   // later unit runs as split_k CTAs over consecutive key-tile ranges, and the last of them to
   // finish merges the parts' partial results
+  const int32_t* perm;  // sparse: CTA i runs unit perm[i] (longest first); null = natural order
   int n_whole;          // = number of units when nothing is split
   int split_k;          // parts per split unit (1 = no split)
   float* ws_part;       // per part and slot: O^T [d][128] then m [128] and l [128], fp32
@@ -72,6 +73,14 @@ struct PoolArgs {
   void* out_lo;          // [B, H, nblk, d] 16-bit round of (mean - hi), may be null
 };
 cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st);
+
+// Longest-first order of the sparse attention's units (see order_units_kernel).
+struct OrderArgs {
+  const int32_t* tile_cnt;  // [B, Hq, n_qt]
+  int B, Hq, n_qt, slots, n_hp, s, U;
+  int32_t* perm;            // [U] out
+};
+cudaError_t launch_order_units(const OrderArgs& o, cudaStream_t st);
 
 struct IndexArgs {
   int ab_type;           // 0 = f16, 1 = bf16 (q and the kbar hi/lo split)

@@ -550,6 +550,22 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   maps.vc = maps.vh;
   if ((rc = map_out(&maps.out, out, sh->out_dtype, B, C, Hq, d, os)) != PF_OK) return rc;
   if (a.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
+  // longest-first unit order, kept in the workspace's spare 16-bit region when it fits
+  const long long units = (long long)a.n_qt * a.n_hp * B;
+  if (units * 4 <= lpb) {
+    OrderArgs o{};
+    o.tile_cnt = sel->tile_cnt;
+    o.B = B;
+    o.Hq = Hq;
+    o.n_qt = a.n_qt;
+    o.slots = a.slots;
+    o.n_hp = a.n_hp;
+    o.s = start_pos;
+    o.U = (int)units;
+    o.perm = reinterpret_cast<int32_t*>(static_cast<char*>(pooled) + f32b);
+    if ((e = launch_order_units(o, st)) != cudaSuccess) return cuda_fail(e, "unit order launch");
+    a.perm = o.perm;
+  }
   if ((e = launch_attn(maps, a, MODE_SPARSE, st)) != cudaSuccess) return cuda_fail(e, "attention launch");
   return PF_OK;
 }

@@ -85,7 +85,73 @@ __global__ void pool_kernel(PoolArgs a, int bf16) {
   }
 }
 
+// Longest-first order of the sparse attention's work units.  Unit u is the one the
+// attention kernel runs as CTA u in its natural order (query tiles from the last);
+// its cost in key tiles is its pooled tiles plus both heads' kept-list lengths (an
+// upper bound on the union it executes).  One CTA counting-sorts the costs
+// descending and writes perm[i] = the i-th heaviest unit, so that the hardware
+// block scheduler hands the heavy units out first.
+constexpr int kOrderBins = 8192;
+__global__ void __launch_bounds__(1024) order_units_kernel(OrderArgs o) {
+  __shared__ int bins[kOrderBins];
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x;
+  auto cost = [&](int u) {
+    const int per_qt = o.n_hp * o.B;
+    const int qt = o.n_qt - 1 - u / per_qt;
+    const int rem = u % per_qt;
+    const int b = rem / o.n_hp;
+    const int h0 = (rem % o.n_hp) * o.slots;
+    const int ob = o.s / 128 + qt;
+    int c = (ob + 127) / 128 + o.tile_cnt[(long long)(b * o.Hq + h0) * o.n_qt + qt];
+    if (o.slots == 2) c += o.tile_cnt[(long long)(b * o.Hq + h0 + 1) * o.n_qt + qt];
+    return min(max(c, 0), kOrderBins - 1);
+  };
+  for (int i = tid; i < kOrderBins; i += blockDim.x) bins[i] = 0;
+  __syncthreads();
+  for (int u = tid; u < o.U; u += blockDim.x) atomicAdd(&bins[cost(u)], 1);
+  __syncthreads();
+  // exclusive scan from the highest cost down: bins[c] = units costing more than c
+  constexpr int per = kOrderBins / 1024;
+  int loc[per], run = 0;
+  const int hi = kOrderBins - 1 - tid * per;  // this thread's bins, descending
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    loc[i] = run;
+    run += bins[hi - i];
+  }
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if ((tid & 31) >= off) incl += v;
+  }
+  if ((tid & 31) == 31) warp_sums[tid >> 5] = incl;
+  __syncthreads();
+  if (tid < 32) {
+    int v = warp_sums[tid];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, off);
+      if (tid >= off) v += t;
+    }
+    warp_sums[tid] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (incl - run) + ((tid >> 5) > 0 ? warp_sums[(tid >> 5) - 1] : 0);
+#pragma unroll
+  for (int i = 0; i < per; ++i) bins[hi - i] = before + loc[i];
+  __syncthreads();
+  for (int u = tid; u < o.U; u += blockDim.x) o.perm[atomicAdd(&bins[cost(u)], 1)] = u;
+}
+
 }  // namespace
+
+cudaError_t launch_order_units(const OrderArgs& o, cudaStream_t st) {
+  order_units_kernel<<<1, 1024, 0, st>>>(o);
+  ++t_launches;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st) {
   dim3 grid(a.nblk, a.B);
