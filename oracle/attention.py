@@ -78,7 +78,7 @@ def causal_additive(C: int, start_pos: int, rows=None) -> np.ndarray:
 # dense chunked prefill
 # --------------------------------------------------------------------------
 def dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, scale=None, rows=None,
-          heads=None):
+          heads=None, with_lse=False):
     """Attention of a chunk over [history ; chunk] keys.
 
     q [B, C, Hq, d]; k_hist, v_hist [B, s, Hkv, d]; k_chunk, v_chunk
@@ -86,7 +86,9 @@ def dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, scale=None,
     None for causal.  For every row i (absolute position p = s + i) and head
     h: l_j = (q_i . k_j) * scale + M[i, j] over all keys j < s + C,
     o_i = sum_j exp(l_j - max l) v_j / sum_j exp(l_j - max l).
-    Returns out [B, len(rows), len(heads), d].
+    Returns out [B, len(rows), len(heads), d]; with with_lse also
+    lse [B, len(rows), len(heads)] = log sum_j exp(l_j), the log of the
+    softmax denominator, which lets results over disjoint key sets be merged.
     """
     B, C, Hq, d = q.shape
     Hkv = k_chunk.shape[2]
@@ -100,6 +102,7 @@ def dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, scale=None,
     rows = _rows_arg(rows, C)
     heads = _heads_arg(heads, Hq)
     out = np.empty((B, len(rows), len(heads), d))
+    lse = np.empty((B, len(rows), len(heads)))
     step = max(1, _ROW_ELEMS // T)
     for b in range(B):
         for hi, h in enumerate(heads):
@@ -111,8 +114,10 @@ def dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, scale=None,
                 logits += causal_additive(C, s, rr) if mask is None else mask[rr, :]
                 m = logits.max(axis=1, keepdims=True)
                 w = np.exp(logits - m)
-                out[b, r0:r0 + len(rr), hi, :] = (w @ vg) / w.sum(axis=1, keepdims=True)
-    return out
+                den = w.sum(axis=1, keepdims=True)
+                out[b, r0:r0 + len(rr), hi, :] = (w @ vg) / den
+                lse[b, r0:r0 + len(rr), hi] = m[:, 0] + np.log(den[:, 0])
+    return (out, lse) if with_lse else out
 
 
 def chunk_kv_cache_layout(k_chunk):
@@ -198,7 +203,8 @@ def tile_union(kept_tile_rows) -> np.ndarray:
 # --------------------------------------------------------------------------
 # block-sparse prefill: exact kept blocks + pooled correction
 # --------------------------------------------------------------------------
-def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, sel=None):
+def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, sel=None,
+           with_lse=False):
     """Block-sparse attention with pooled correction.
 
     Row i (p = s + i), head h: kept set K_i from ``block_select``; skipped set
@@ -207,7 +213,8 @@ def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, 
       m = max(max_E l_j, max_R s_ib)
       o_i = (sum_E e^(l_j - m) v_j + sum_R n_b e^(s_ib - m) vbar_b)
             / (sum_E e^(l_j - m) + sum_R n_b e^(s_ib - m)).
-    Returns (out [B, R, Hsel, d], sel).
+    Returns (out [B, R, Hsel, d], sel); with with_lse also lse [B, R, Hsel], the
+    log of the denominator above (exact and pooled terms).
     """
     B, N, Hq, d = q.shape
     T, Hkv = k.shape[1], k.shape[2]
@@ -222,6 +229,7 @@ def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, 
     nb = block_counts(T, block)
     nblk = len(nb)
     out = np.empty((B, len(rows), len(heads), d))
+    lse = np.empty((B, len(rows), len(heads)))
     p_all = s + rows
     ob_all = p_all // block
     jblk = np.arange(T) // block
@@ -244,7 +252,8 @@ def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, 
                 num = we @ vg + wp @ vbar[b, g]
                 den = we.sum(axis=1) + wp.sum(axis=1)
                 out[b, sl, hi, :] = num / den[:, None]
-    return out, sel
+                lse[b, sl, hi] = m[:, 0] + np.log(den)
+    return (out, sel, lse) if with_lse else (out, sel)
 
 
 def skip_share(sel: Selection) -> float:

@@ -7,7 +7,11 @@
 * the block-sparse path: alpha = 0 and block-constant keys reduce it to dense
   causal attention; a hand-worked 36-token toy fixes the selection and a
   hand-derived row fixes the pooled-correction weight n_b * e^(s_b) and vbar_b;
-* the folded-indexer mask's visible-key budget 512*4 + 3 = 2051.
+* the folded-indexer mask's visible-key budget 512*4 + 3 = 2051;
+* the log-sum-exp output: identical keys give q.k0 * scale + log(visible count),
+  a mask shift moves it by the same constant, results over disjoint key sets
+  merge through it into the full result, and the toy's hand-derived
+  denominator fixes the sparse one.
 """
 import json
 import math
@@ -318,3 +322,65 @@ def test_sparse_negative_control():
     b, _ = oracle.sparse(q, k, v, 0, 64, 0.0, rows=rows)
     assert oracle.skip_share(sel) > 0.5
     assert np.max(np.abs(a - b)) > 10 * 5e-3
+
+
+# --------------------------------------------------------------------------- log-sum-exp
+def test_lse_identical_keys_closed_form():
+    """Every key equal to k0: row i sees s + i + 1 keys, so lse = q.k0 * scale + log(s + i + 1)."""
+    g = np.random.default_rng(40)
+    B, C, s, Hq, Hkv, d = 1, 6, 5, 2, 1, 8
+    q = g.standard_normal((B, C, Hq, d))
+    k0 = g.standard_normal(d)
+    kh = np.broadcast_to(k0, (B, s, Hkv, d)).copy()
+    kc = np.broadcast_to(k0, (B, C, Hkv, d)).copy()
+    v = g.standard_normal((B, s + C, Hkv, d))
+    _, lse = oracle.dense(q, kh, v[:, :s], kc, v[:, s:], s, with_lse=True)
+    scale = 1.0 / math.sqrt(d)
+    for i in range(C):
+        for h in range(Hq):
+            assert abs(lse[0, i, h] - (float(q[0, i, h] @ k0) * scale + math.log(s + i + 1))) <= 1e-12
+
+
+def test_lse_shifts_with_the_mask():
+    q, kh, vh, kc, vc = rand_case(41)
+    C, s = q.shape[1], kh.shape[1]
+    mask = np.where(np.random.default_rng(42).random((C, s + C)) < 0.3, -30000.0, 0.0)
+    out0, lse0 = oracle.dense(q, kh, vh, kc, vc, s, mask=mask, with_lse=True)
+    out1, lse1 = oracle.dense(q, kh, vh, kc, vc, s, mask=mask + 2.5, with_lse=True)
+    assert np.max(np.abs(lse1 - lse0 - 2.5)) <= 1e-12
+    assert np.max(np.abs(out1 - out0)) <= 1e-12
+
+
+def test_lse_merges_disjoint_key_sets():
+    """Split-KV identity: attention over history and over the chunk separately, merged
+    through their log-sum-exps, is attention over both."""
+    q, kh, vh, kc, vc = rand_case(43)
+    C, s = q.shape[1], kh.shape[1]
+    full, lse = oracle.dense(q, kh, vh, kc, vc, s, with_lse=True)
+    causal = oracle.causal_additive(C, s)
+    hist_only = causal.copy()
+    hist_only[:, s:] = -30000.0
+    chunk_only = causal.copy()
+    chunk_only[:, :s] = -30000.0
+    oa, la = oracle.dense(q, kh, vh, kc, vc, s, mask=hist_only, with_lse=True)
+    ob, lb = oracle.dense(q, kh, vh, kc, vc, s, mask=chunk_only, with_lse=True)
+    merged_lse = np.logaddexp(la, lb)
+    merged = (np.exp(la - merged_lse)[..., None] * oa + np.exp(lb - merged_lse)[..., None] * ob)
+    assert np.max(np.abs(merged_lse - lse)) <= 1e-12
+    assert np.max(np.abs(merged - full)) <= 1e-12
+
+
+def test_sparse_lse_toy36_closed_form():
+    """Row 12 of the toy (kept {1, 2}, block 0 pooled with weight 6 and logit 0): the
+    denominator is 3e^3.5 + 3e^2.5 + e^1.5 + 6."""
+    q, k, v, blk, scale = toy36()
+    _, _, lse = oracle.sparse(q, k, v, 0, blk, 0.2, scale=scale, rows=[12], with_lse=True)
+    den = 3 * math.exp(3.5) + 3 * math.exp(2.5) + math.exp(1.5) + 6.0
+    assert abs(lse[0, 0, 0] - math.log(den)) <= 1e-13
+
+
+def test_sparse_lse_alpha_zero_equals_dense():
+    q, k, v, s = sparse_case(44)
+    _, dlse = oracle.dense(q, k[:, :s], v[:, :s], k[:, s:], v[:, s:], s, with_lse=True)
+    _, _, slse = oracle.sparse(q, k, v, s, 8, 0.0, with_lse=True)
+    assert np.max(np.abs(slse - dlse)) <= 1e-12
