@@ -100,6 +100,10 @@ typedef struct {
  * out_k / out_v (optional, both or neither): bit copies of k_chunk / v_chunk
  * written at okv_stride, by default head-major [B, Hkv, C, d], so a caller can
  * point them at row start_pos of its own cache.
+ * lse (optional, [B, Hq, C] fp32, contiguous, 4-byte aligned): the natural log
+ * of each row's softmax denominator, log sum_j exp(l_j); results over disjoint
+ * key sets (e.g. a short chunk split across a long history) merge as
+ * lse = logaddexp(lse_a, lse_b), out = e^(lse_a - lse) out_a + e^(lse_b - lse) out_b.
  * workspace (optional, device memory owned by the caller, 16-byte aligned,
  * workspace_bytes >= pf_dense_workspace_bytes, PF_EINVAL otherwise): lets the
  * call split the key range of its last, partial wave of work units across the
@@ -113,8 +117,9 @@ typedef struct {
  */
 pf_status pf_attn_dense(const pf_shape* shape, const void* q, const void* k_hist,
                         const void* v_hist, const void* k_chunk, const void* v_chunk,
-                        const void* mask, int32_t start_pos, void* out, void* out_k,
-                        void* out_v, void* workspace, int64_t workspace_bytes, void* stream);
+                        const void* mask, int32_t start_pos, void* out, float* lse,
+                        void* out_k, void* out_v, void* workspace, int64_t workspace_bytes,
+                        void* stream);
 
 /* Bytes of the optional pf_attn_dense workspace for shape->d on the current
  * device (about 20 MB for d = 128 on 152 SMs; independent of the sequence). */
@@ -162,11 +167,12 @@ pf_status pf_block_index(const pf_shape* shape, const void* q, const void* k, in
  * pooled: caller-allocated workspace of pf_sparse_sizes.pooled_bytes; on
  * return it starts with vbar, the fp32 block means of v, [B, Hkv, nblk, d];
  * the rest is scratch.  sel must come from pf_block_index on the same q, k,
- * start_pos and block.
+ * start_pos and block.  lse (optional, [B, Hq, C] fp32): the log of the
+ * denominator above, exact and pooled terms, as for pf_attn_dense.
  */
 pf_status pf_attn_sparse(const pf_shape* shape, const void* q, const void* k, const void* v,
                          int32_t start_pos, int32_t block, const pf_sel* sel, void* pooled,
-                         void* out, void* stream);
+                         void* out, float* lse, void* stream);
 
 /*
  * pf_attn_sparse_static -- pf_attn_sparse for callers that cannot allocate
@@ -197,7 +203,7 @@ pf_status pf_attn_sparse(const pf_shape* shape, const void* q, const void* k, co
 
 pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void* k,
                                 const void* v, int32_t start_pos, int32_t block,
-                                const pf_sel* sel, void* out, void* stream);
+                                const pf_sel* sel, void* out, float* lse, void* stream);
 
 /* Synchronise `stream`, then report (and clear) a device-side error: PF_ETIMEOUT
  * if a bounded wait in a kernel gave up since the last check; PF_ERANGE if a

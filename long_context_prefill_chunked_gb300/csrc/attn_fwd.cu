@@ -595,11 +595,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (ok)
       ok = wait_all(BAR(B_OF), 0, a.timeout, abort_flag, a.status, (R_SOFT << 8) | B_OF);
     const long long obase = (long long)b * a.o_sb + (long long)row * a.o_st + (long long)h * a.o_sh;
+    // natural log of the softmax denominator: sum_j 2^(y_j) = 2^m * l in the log2 domain
+    auto write_lse = [&](float mm, float ll) {
+      if (a.lse != nullptr && valid)
+        a.lse[((long long)b * a.Hq + h) * a.C + row] = (mm + __log2f(ll)) * 0.6931471805599453f;
+    };
     if (split < 0 && MODE == MODE_SPARSE) {
       // Sparse units are short (tens of tiles): direct row stores keep this mode's loop
       // registers (a staged tile store measured slower here).
       if (ok) {
         tc_fence_after();
+        write_lse(m, l);
         const float inv = 1.f / l;
         for (int c0 = 0; c0 < a.d; c0 += 32) {
           uint32_t o[32];
@@ -622,6 +628,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint8_t* stage = smem + SM_Q + 65536u * sl;
       if (ok) {
         tc_fence_after();
+        write_lse(m, l);
         const float inv = 1.f / l;
         for (int bx = 0; bx < nbox; ++bx) {
           uint32_t wv[32];
@@ -697,6 +704,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             L += wgt[p] * __ldcg(p0 + p * 2 * pstride + (long long)(a.d + 1) * kTile + r);
           }
         }
+        write_lse(M, L);
         const float inv = 1.f / L;
         for (int c0 = 0; c0 < a.d; c0 += 32) {
           float v[32];

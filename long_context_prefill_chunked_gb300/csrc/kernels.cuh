@@ -28,6 +28,7 @@ struct AttnArgs {
   long long mask_ld;    // elements between mask rows
   // output
   void* out;
+  float* lse;           // [B, Hq, C] log of each row's softmax denominator, or null
   int out_dtype;        // 0 f16, 1 bf16, 2 f32
   long long o_sb, o_st, o_sh;
   // block-sparse selection (MODE_SPARSE)

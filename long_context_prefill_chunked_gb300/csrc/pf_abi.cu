@@ -274,8 +274,8 @@ pf_status pf_dense_workspace_bytes(const pf_shape* sh, int64_t* bytes) {
 
 pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, const void* v_hist,
                         const void* k_chunk, const void* v_chunk, const void* mask,
-                        int32_t start_pos, void* out, void* out_k, void* out_v, void* workspace,
-                        int64_t workspace_bytes, void* stream) {
+                        int32_t start_pos, void* out, float* lse, void* out_k, void* out_v,
+                        void* workspace, int64_t workspace_bytes, void* stream) {
   pf_status rc = check_common(sh, start_pos);
   if (rc != PF_OK) return rc;
   if (q == nullptr || k_chunk == nullptr || v_chunk == nullptr || out == nullptr)
@@ -292,6 +292,8 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
       return fail(PF_EINVAL, "workspace of %lld bytes is smaller than pf_dense_workspace_bytes (%lld)",
                   (long long)workspace_bytes, dense_workspace_bytes(sh->d, P));
   }
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0u)
+    return fail(PF_EINVAL, "lse must be 4-byte aligned");
   const void* ptrs[] = {q, k_hist, v_hist, k_chunk, v_chunk, out, out_k, out_v, workspace};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return fail(PF_EINVAL, "every base pointer must be 16-byte aligned");
@@ -316,6 +318,7 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
   fill_attn_common(sh, start_pos, a);
   a.n_hist_tiles = s / kTile;
   a.out = out;
+  a.lse = lse;
   a.o_sb = os[0];
   a.o_st = os[1];
   a.o_sh = os[2];
@@ -476,7 +479,9 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
 
 pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const void* v,
                          int32_t start_pos, int32_t block, const pf_sel* sel, void* pooled,
-                         void* out, void* stream) {
+                         void* out, float* lse, void* stream) {
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0u)
+    return fail(PF_EINVAL, "lse must be 4-byte aligned");
   long long ks[3], qs[3], os[3];
   pf_sparse_sizes z;
   pf_status rc = check_sparse(sh, start_pos, block, ks, qs, &z);
@@ -523,6 +528,7 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   fill_attn_common(sh, start_pos, a);
   a.n_hist_tiles = 1 << 30;  // every exact key tile comes from the one K/V cache map
   a.out = out;
+  a.lse = lse;
   a.o_sb = os[0];
   a.o_st = os[1];
   a.o_sh = os[2];

@@ -62,7 +62,7 @@ extern "C" {
 
 pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void* k, const void* v,
                                 int32_t start_pos, int32_t block, const pf_sel* sel, void* out,
-                                void* stream) {
+                                float* lse, void* stream) {
   pf_sparse_sizes z;
   pf_status rc = pf_sparse_query_sizes(shape, start_pos, block, &z);
   if (rc != PF_OK) return rc;
@@ -85,7 +85,7 @@ pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void
   }
   // Every byte of the workspace that the kernels read is written earlier in
   // the same call, so stale contents from a previous call do not matter.
-  return pf_attn_sparse(shape, q, k, v, start_pos, block, sel, scratch, out, stream);
+  return pf_attn_sparse(shape, q, k, v, start_pos, block, sel, scratch, out, lse, stream);
 }
 
 }  // extern "C"

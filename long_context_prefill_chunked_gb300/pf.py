@@ -72,10 +72,10 @@ def load() -> ctypes.CDLL:
         raise ImportError("libpf.so not found at %s: run __graft_entry__.build() first" % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     V, I32, I64, F, P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.POINTER
-    lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V, I64, V]
+    lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V, V, I64, V]
     lib.pf_dense_workspace_bytes.argtypes = [P(Shape), P(I64)]
     lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(Sel), V]
-    lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V]
+    lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V, V]
     lib.pf_sparse_query_sizes.argtypes = [P(Shape), I32, I32, P(SparseSizes)]
     lib.pf_stream_status.argtypes = [V]
     lib.pf_set_wait_timeout.argtypes = [I64]
@@ -136,6 +136,14 @@ def _expect_selection(sel, z, B, C, Hq, Hkv, d, device):
     _expect(sel.kbar, (2, B, Hkv, z.nblk, d), "sel.kbar", device)
 
 
+def _expect_lse(lse, B, Hq, C, device):
+    if lse is None:
+        return
+    _expect(lse, (B, Hq, C), "lse", device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, Hq, C] tensor")
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -175,10 +183,11 @@ def dense_workspace(q, stream=None) -> torch.Tensor:
 
 
 def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=None, out_k=None,
-               out_v=None, out_dtype=torch.float32, scale=0.0, stream=None, workspace=True):
+               out_v=None, out_dtype=torch.float32, scale=0.0, stream=None, workspace=True, lse=None):
     """Dense chunked prefill (pf_attn_dense); returns out [B, C, Hq, d].  workspace: True
     uses a cached per-(device, stream) buffer (tail split on), None runs every unit whole,
-    or a caller-owned uint8 tensor of at least pf_dense_workspace_bytes."""
+    or a caller-owned uint8 tensor of at least pf_dense_workspace_bytes.  lse: an optional
+    fp32 [B, Hq, C] tensor that receives log sum_j exp(l_j) per row."""
     lib = load()
     if q.dim() != 4:
         raise ValueError("q must be [B, C, Hq, d]")
@@ -200,6 +209,7 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
         _expect(out_v, (B, Hkv, C, d), "out_v", dev)
     if mask is not None:
         _expect(mask, (C, start_pos + C), "mask", dev)
+    _expect_lse(lse, B, Hq, C, dev)
     if workspace is True:
         workspace = dense_workspace(q, stream)
     elif workspace is False:
@@ -227,8 +237,8 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
         sh.mask_ld = mask.stride(0)
     _check(lib.pf_attn_dense(ctypes.byref(sh), _ptr(q), _ptr(k_hist if start_pos > 0 else None),
                              _ptr(v_hist if start_pos > 0 else None), _ptr(k_chunk), _ptr(v_chunk),
-                             _ptr(mask), int(start_pos), _ptr(out), _ptr(out_k), _ptr(out_v),
-                             _ptr(workspace), int(ws_bytes), _stream(stream)))
+                             _ptr(mask), int(start_pos), _ptr(out), _ptr(lse), _ptr(out_k),
+                             _ptr(out_v), _ptr(workspace), int(ws_bytes), _stream(stream)))
     return out
 
 
@@ -294,8 +304,9 @@ def alloc_pooled(q, k, start_pos, block=128) -> torch.Tensor:
 
 
 def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=None,
-                out_dtype=torch.float32, scale=0.0, stream=None):
-    """Block-sparse attention with pooled correction (pf_attn_sparse); returns out."""
+                out_dtype=torch.float32, scale=0.0, stream=None, lse=None):
+    """Block-sparse attention with pooled correction (pf_attn_sparse); returns out.  lse:
+    an optional fp32 [B, Hq, C] tensor for the log of each row's denominator."""
     lib = load()
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q must be [B, C, Hq, d] and k, v [B, start_pos + C, Hkv, d]")
@@ -309,6 +320,7 @@ def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=
     if out is None:
         out = torch.empty((B, C, Hq, d), dtype=out_dtype, device=q.device)
     _expect(out, (B, C, Hq, d), "out", dev)
+    _expect_lse(lse, B, Hq, C, dev)
     if pooled is None:
         pooled = alloc_pooled(q, k, start_pos, block)
     if pooled.device != dev or pooled.numel() * pooled.element_size() < z.pooled_bytes:
@@ -320,7 +332,7 @@ def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=
     sh.o_stride = _bth(out)
     cs = sel.c_struct()
     _check(lib.pf_attn_sparse(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), int(start_pos), int(block),
-                              ctypes.byref(cs), _ptr(pooled), _ptr(out), _stream(stream)))
+                              ctypes.byref(cs), _ptr(pooled), _ptr(out), _ptr(lse), _stream(stream)))
     return out
 
 

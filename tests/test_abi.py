@@ -53,7 +53,7 @@ MISALIGNED = ctypes.c_void_p(0x100008)
 def dense(lib, sh, q=FAKE, kh=None, vh=None, kc=FAKE, vc=FAKE, mask=None, s=0, out=FAKE, ok=None, ov=None,
           ws=None, ws_bytes=0):
     return lib.pf_attn_dense(ctypes.byref(sh) if sh is not None else None, q, kh, vh, kc, vc, mask, s,
-                             out, ok, ov, ws, ws_bytes, None)
+                             out, None, ok, ov, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -89,9 +89,9 @@ def test_sparse_rejects_bad_arguments(lib):
     assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, 1.5, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
     assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, -0.1, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
     assert lib.pf_block_index(ctypes.byref(sh), None, FAKE, 0, 128, 0.1, ctypes.byref(sel), None) == pf.PF_EINVAL
-    assert lib.pf_attn_sparse(ctypes.byref(sh), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), None, FAKE, None) == pf.PF_EINVAL
+    assert lib.pf_attn_sparse(ctypes.byref(sh), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), None, FAKE, None, None) == pf.PF_EINVAL
     long = shape(C=300000)
-    assert lib.pf_attn_sparse(ctypes.byref(long), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), FAKE, FAKE, None) == pf.PF_EUNSUPPORTED
+    assert lib.pf_attn_sparse(ctypes.byref(long), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), FAKE, FAKE, None, None) == pf.PF_EUNSUPPORTED
 
 
 def test_sparse_sizes(lib):

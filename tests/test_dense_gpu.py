@@ -212,3 +212,27 @@ def test_tail_split_workspace_too_small_is_refused():
     with pytest.raises(pfx.PFError) as e:
         pfx.attn_dense(q, kh, vh, kc, vc, 512, workspace=torch.empty(1024, dtype=torch.uint8, device="cuda"))
     assert e.value.status == pf.PF_EINVAL
+
+
+# --------------------------------------------------------------------------- log-sum-exp
+LSE_TOL = 1e-4   # fp32 scores and sums, ex2/lg2 approximations: ~1e-6 relative on |lse| ~ 10
+
+
+@pytest.mark.parametrize("case", ["causal", "mask", "split"])
+def test_lse_matches_oracle(case):
+    C, s = 1024, 2048
+    w = pi.normal_workload("lse-" + case, 71, 1, 8, 2, 128, s + C, C, "bf16")
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(s))
+    mask = None
+    if case == "mask":
+        mask = np.zeros((C, s + C), dtype=np.float32)
+        mask[np.random.default_rng(72).random(mask.shape) < 0.3] = -30000.0
+    lse = torch.empty((1, 8, C), dtype=torch.float32, device="cuda")
+    out = pfx.attn_dense(q, kh, vh, kc, vc, s, mask=None if mask is None else torch.from_numpy(mask).cuda(),
+                         lse=lse, workspace=True if case == "split" else None)
+    pfx.stream_status()
+    ref, rlse = oracle.dense(*(w.f64(x) for x in w.chunk_views(s)), s,
+                             mask=None if mask is None else mask.astype(np.float64), with_lse=True)
+    assert_close(out, ref, "lse case " + case)
+    got = lse.cpu().double().numpy().transpose(0, 2, 1)          # [B, C, Hq]
+    assert np.max(np.abs(got - rlse)) <= LSE_TOL, np.max(np.abs(got - rlse))

@@ -165,3 +165,27 @@ def test_config5_128k_last_chunk_sampled_rows():
     dref = oracle.dense(w.f64(w.q[:, s:]), w.f64(w.k[:, :s]), w.f64(w.v[:, :s]), w.f64(w.k[:, s:]),
                         w.f64(w.v[:, s:]), s, rows=rows[:128])
     assert_close(dense[:, rows[:128]], dref, "dense 128K last chunk")
+
+
+def test_sparse_lse_matches_oracle(small):
+    """lse = log of the row's denominator (exact and pooled terms).  Exact keys: within
+    1e-4 (fp32 scores and sums).  Pooled terms score q against kbar rounded to the input
+    type (bf16: 2^-9 relative), and lse moves by at most the largest logit error, so with
+    skipped blocks the bound adds 2^-9 * max |pooled logit|."""
+    w = small
+    s, C = 1024, 1024
+    q = dev(w.q[:, s:s + C], w.dtype)
+    k = dev(w.k[:, :s + C], w.dtype)
+    v = dev(w.v[:, :s + C], w.dtype)
+    for alpha in (0.0, 0.1):
+        sel = pfx.block_index(q, k, s, 128, alpha)
+        lse = torch.empty((1, q.shape[2], C), dtype=torch.float32, device="cuda")
+        pfx.attn_sparse(q, k, v, s, sel, lse=lse)
+        pfx.stream_status()
+        _, osel, rlse = oracle.sparse(w.f64(w.q[:, s:s + C]), w.f64(w.k[:, :s + C]), w.f64(w.v[:, :s + C]),
+                                      s, 128, alpha, with_lse=True)
+        ok = ~osel.near
+        got = lse.cpu().double().numpy().transpose(0, 2, 1)
+        pooled_max = np.abs(np.where(np.isfinite(osel.scores), osel.scores, 0.0)).max()
+        tol = 1e-4 if alpha == 0.0 else 1e-4 + 2.0 ** -9 * pooled_max
+        assert np.max(np.abs(got - rlse)[ok]) <= tol, (alpha, np.max(np.abs(got - rlse)[ok]), tol)

@@ -26,7 +26,7 @@ def lib():
     fn = lib.pf_attn_sparse_static
     V = ctypes.c_void_p
     fn.argtypes = [ctypes.POINTER(pf.Shape), V, V, V, ctypes.c_int32, ctypes.c_int32,
-                   ctypes.POINTER(pf.Sel), V, V]
+                   ctypes.POINTER(pf.Sel), V, V, V]
     fn.restype = ctypes.c_int
     return lib
 
@@ -39,7 +39,8 @@ def call_static(lib, q, k, v, s, sel, out):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return lib.pf_attn_sparse_static(ctypes.byref(sh), ctypes.c_void_p(q.data_ptr()),
                                      ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
-                                     s, 128, ctypes.byref(cs), ctypes.c_void_p(out.data_ptr()), stream)
+                                     s, 128, ctypes.byref(cs), ctypes.c_void_p(out.data_ptr()), None,
+                                     stream)
 
 
 def test_static_scratch_matches_caller_workspace_two_calls(lib):
@@ -64,6 +65,7 @@ def test_static_scratch_refuses_oversized_problems(lib):
     sh.in_dtype, sh.out_dtype, sh.mask_dtype = pf.PF_BF16, pf.PF_F32, pf.PF_F32
     fake = ctypes.c_void_p(0x100000)
     sel = pf.Sel(0x100000, 0x100000, 0x100000, 0x100000)
-    rc = lib.pf_attn_sparse_static(ctypes.byref(sh), fake, fake, fake, 0, 128, ctypes.byref(sel), fake, None)
+    rc = lib.pf_attn_sparse_static(ctypes.byref(sh), fake, fake, fake, 0, 128, ctypes.byref(sel), fake, None,
+                                   None)
     assert rc == pf.PF_EUNSUPPORTED
     assert b"static buffer" in lib.pf_last_error()
