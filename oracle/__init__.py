@@ -4,8 +4,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 and reference legs may import this package.  It shares no code with the CUDA
 library and never calls it.
 """
-from .attention import (MASK_DROP, Selection, block_counts, block_select, causal_additive,
-                        chunk_kv_cache_layout, dense, pool_blocks, skip_share, sparse, tile_union)
+from .attention import (MASK_DROP, KeepRules, Selection, block_counts, block_select,
+                        causal_additive, chunk_kv_cache_layout, dense, pool_blocks, skip_share,
+                        sparse, tile_union)
 
-__all__ = ["MASK_DROP", "Selection", "block_counts", "block_select", "causal_additive",
+__all__ = ["MASK_DROP", "KeepRules", "Selection", "block_counts", "block_select", "causal_additive",
            "chunk_kv_cache_layout", "dense", "pool_blocks", "skip_share", "sparse", "tile_union"]

@@ -155,15 +155,38 @@ class Selection:
     block: int
 
 
+@dataclasses.dataclass(frozen=True)
+class KeepRules:
+    """Keep rules of the Metal port ("Porting FlashPrefill V2 to Apple silicon for faster
+    prefill", the selection-map figure in "At 16k, only 28% of visible blocks run in
+    full"): sinks, a local window and a dense tail are kept by rule; selection runs per
+    32-position query tile; the map is per KV head.  Readings: a sink covers the blocks
+    holding keys j < sink_tokens; the window is the local_blocks candidates just below
+    the diagonal (the figure gives no width); the dense tail is the rows at positions
+    p >= T - dense_tail_rows (T = start_pos + N, the end of the keys this call sees);
+    a query tile's selection is the union of its rows' (each row keeps its own
+    candidates only); a KV head's selection is the union of its query heads'."""
+    sink_tokens: int = 0
+    local_blocks: int = 0
+    dense_tail_rows: int = 0
+    row_group: int = 1
+    share_kv_group: bool = False
+
+
 def block_select(q, k, start_pos, block, alpha, scale=None, rows=None, heads=None,
-                 near_rel=1e-4) -> Selection:
+                 near_rel=1e-4, rules=None) -> Selection:
     """Per-row block selection.
 
     q [B, N, Hq, d] (the chunk's queries), k [B, s + N, Hkv, d] (all keys).
     For row i at p = s + i: ob = floor(p / block); candidates b < ob;
     s_ib = (q_i . kbar_b) * scale; keep candidate b iff
     exp(s_ib - max_c s_ic) >= alpha; the diagonal block ob is always kept.
+    rules (KeepRules): applied in order -- per-row rule keeps (sinks, window,
+    dense tail), the union over aligned groups of row_group positions, the union
+    over the query heads of a KV head; a group with a near row is near.
     """
+    if rules is not None and (rules.row_group > 1 or rules.share_kv_group):
+        return _select_grouped(q, k, start_pos, block, alpha, scale, rows, heads, near_rel, rules)
     B, N, Hq, d = q.shape
     T, Hkv = k.shape[1], k.shape[2]
     G = Hq // Hkv
@@ -188,11 +211,50 @@ def block_select(q, k, start_pos, block, alpha, scale=None, rows=None, heads=Non
             diff = np.where(cand, sc - np.where(has[:, None], smax, 0.0), -np.inf)
             ratio = np.exp(diff)                                      # p_b / p_max
             keep = cand & (ratio >= alpha)
+            if rules is not None:
+                bidx = np.arange(nblk)[None, :]
+                keep |= cand & (bidx * block < rules.sink_tokens)
+                keep |= cand & (bidx >= ob[:, None] - rules.local_blocks)
+                keep |= cand & ((s + rows)[:, None] >= s + N - rules.dense_tail_rows)
             keep[np.arange(len(rows)), ob] = True
             kept[b, :, hi] = keep
             if alpha > 0:
                 near[b, :, hi] = (cand & (np.abs(ratio - alpha) <= near_rel * alpha)).any(axis=1)
     return Selection(kbar, kept, near, scores, rows, heads, s, block)
+
+
+def _select_grouped(q, k, start_pos, block, alpha, scale, rows, heads, near_rel, rules):
+    """block_select with the group unions: selects every row and head of the groups that
+    the requested rows and heads belong to, takes the unions, returns the requested ones."""
+    B, N, Hq, _ = q.shape
+    G = Hq // k.shape[2]
+    s = int(start_pos)
+    rows = _rows_arg(rows, N)
+    heads = _heads_arg(heads, Hq)
+    g_rows = rules.row_group if rules.row_group > 1 else 1
+    all_rows = np.arange(N)
+    all_heads = list(range(Hq))
+    base_rules = dataclasses.replace(rules, row_group=1, share_kv_group=False)
+    full = block_select(q, k, s, block, alpha, scale, all_rows, all_heads, near_rel, base_rules)
+    kept, near = full.kept.copy(), full.near.copy()
+    ob = (s + all_rows) // block
+    cand = np.arange(kept.shape[-1])[None, :] < ob[:, None]
+    if g_rows > 1:
+        grp = (s + all_rows) // g_rows
+        for gi in np.unique(grp):
+            m = grp == gi
+            u = kept[:, m].any(axis=1, keepdims=True)              # [B, 1, Hq, nblk]
+            kept[:, m] |= u & cand[m][None, :, None, :]
+            near[:, m] |= near[:, m].any(axis=1, keepdims=True)
+    if rules.share_kv_group:
+        for g in range(Hq // G):
+            hs = slice(g * G, (g + 1) * G)
+            u = kept[:, :, hs].any(axis=2, keepdims=True)
+            kept[:, :, hs] |= u
+            near[:, :, hs] |= near[:, :, hs].any(axis=2, keepdims=True)
+    hi = np.array(heads)
+    return Selection(full.kbar, kept[:, rows][:, :, hi], near[:, rows][:, :, hi],
+                     full.scores[:, rows][:, :, hi], rows, heads, s, block)
 
 
 def tile_union(kept_tile_rows) -> np.ndarray:
@@ -204,7 +266,7 @@ def tile_union(kept_tile_rows) -> np.ndarray:
 # block-sparse prefill: exact kept blocks + pooled correction
 # --------------------------------------------------------------------------
 def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, sel=None,
-           with_lse=False):
+           with_lse=False, rules=None):
     """Block-sparse attention with pooled correction.
 
     Row i (p = s + i), head h: kept set K_i from ``block_select``; skipped set
@@ -223,7 +285,7 @@ def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, 
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if sel is None:
-        sel = block_select(q, k, s, block, alpha, scale, rows, heads)
+        sel = block_select(q, k, s, block, alpha, scale, rows, heads, rules=rules)
     rows, heads = sel.rows, sel.heads
     vbar = pool_blocks(v, block)
     nb = block_counts(T, block)

@@ -11,7 +11,11 @@
 * the log-sum-exp output: identical keys give q.k0 * scale + log(visible count),
   a mask shift moves it by the same constant, results over disjoint key sets
   merge through it into the full result, and the toy's hand-derived
-  denominator fixes the sparse one.
+  denominator fixes the sparse one;
+* the keep rules: the toy's golden lists extended by hand for sinks, a local
+  window and a dense tail, hand-worked unions for 2-row groups and for a KV
+  group of two query heads, sharing as a no-op without groups, and dense-tail
+  rows reducing to plain causal attention.
 """
 import json
 import math
@@ -384,3 +388,79 @@ def test_sparse_lse_alpha_zero_equals_dense():
     _, dlse = oracle.dense(q, k[:, :s], v[:, :s], k[:, s:], v[:, s:], s, with_lse=True)
     _, _, slse = oracle.sparse(q, k, v, s, 8, 0.0, with_lse=True)
     assert np.max(np.abs(slse - dlse)) <= 1e-12
+
+
+# --------------------------------------------------------------------------- keep rules
+def _toy_kept(sel, blk=6, head=0):
+    return [np.flatnonzero(sel.kept[0, qb * blk, head]).tolist() for qb in range(6)]
+
+
+def test_keep_rules_off_equal_the_base_rule():
+    q, k, v, s = sparse_case(50)
+    a = oracle.block_select(q, k, s, 8, 0.1)
+    b = oracle.block_select(q, k, s, 8, 0.1, rules=oracle.KeepRules())
+    assert np.array_equal(a.kept, b.kept)
+
+
+def test_toy36_sinks_window_and_tail_by_hand():
+    """From the alpha 0.2 golden lists: a 6-token sink adds block 0, a one-block window
+    adds block qb-1, a 6-row dense tail makes the last query block keep every candidate."""
+    q, k, v, blk, scale = toy36()
+    sink = oracle.block_select(q, k, 0, blk, 0.2, scale=scale, rules=oracle.KeepRules(sink_tokens=6))
+    assert _toy_kept(sink) == [[0], [0, 1], [0, 1, 2], [0, 1, 3], [0, 1, 3, 4], [0, 1, 3, 5]]
+    win = oracle.block_select(q, k, 0, blk, 0.2, scale=scale, rules=oracle.KeepRules(local_blocks=1))
+    assert _toy_kept(win) == [[0], [0, 1], [1, 2], [1, 2, 3], [1, 3, 4], [1, 3, 4, 5]]
+    tail = oracle.block_select(q, k, 0, blk, 0.2, scale=scale, rules=oracle.KeepRules(dense_tail_rows=6))
+    assert _toy_kept(tail) == [[0], [0, 1], [1, 2], [1, 3], [1, 3, 4], [0, 1, 2, 3, 4, 5]]
+    assert np.flatnonzero(tail.kept[0, 29, 0]).tolist() == [1, 3, 4]   # row 29 is not in the tail
+
+
+def _toy_two_signs():
+    """The toy's keys with two queries: +(2,0,0,0) scores the blocks t_b, -(2,0,0,0) scores
+    -t_b = (0, -3, -1, -2.5, -0.5, 1).  At alpha 0.2, in query block 4 (candidates 0..3) the
+    first keeps {1, 3} (t >= 3 - 1.609) and the second keeps {0, 2} (-t >= 0 - 1.609)."""
+    q, k, v, blk, scale = toy36()
+    q2 = np.concatenate([q, -q], axis=2)                      # two query heads, one KV head
+    return q2, k, v, blk, scale
+
+
+def test_rows_grouped_take_the_union_by_hand():
+    q2, k, v, blk, scale = _toy_two_signs()
+    q = q2.copy()
+    q[0, 25, 0] = -q2[0, 25, 0]                              # row 25 of head 0 scores -t_b
+    sel = oracle.block_select(q[:, :, :1], k, 0, blk, 0.2, scale=scale)
+    assert np.flatnonzero(sel.kept[0, 24, 0]).tolist() == [1, 3, 4]
+    assert np.flatnonzero(sel.kept[0, 25, 0]).tolist() == [0, 2, 4]
+    grp = oracle.block_select(q[:, :, :1], k, 0, blk, 0.2, scale=scale,
+                              rules=oracle.KeepRules(row_group=2))
+    for r in (24, 25):
+        assert np.flatnonzero(grp.kept[0, r, 0]).tolist() == [0, 1, 2, 3, 4]
+    assert np.flatnonzero(grp.kept[0, 26, 0]).tolist() == [1, 3, 4]      # rows 26, 27 untouched
+
+
+def test_kv_group_shares_the_union_by_hand():
+    q2, k, v, blk, scale = _toy_two_signs()
+    alone = oracle.block_select(q2, k, 0, blk, 0.2, scale=scale)
+    assert np.flatnonzero(alone.kept[0, 24, 1]).tolist() == [0, 2, 4]
+    shared = oracle.block_select(q2, k, 0, blk, 0.2, scale=scale,
+                                 rules=oracle.KeepRules(share_kv_group=True))
+    for h in (0, 1):
+        assert np.flatnonzero(shared.kept[0, 24, h]).tolist() == [0, 1, 2, 3, 4]
+
+
+def test_kv_group_sharing_is_a_no_op_without_groups():
+    q, k, v, s = sparse_case(51, Hq=2, Hkv=2)
+    a = oracle.block_select(q, k, s, 8, 0.1)
+    b = oracle.block_select(q, k, s, 8, 0.1, rules=oracle.KeepRules(share_kv_group=True))
+    assert np.array_equal(a.kept, b.kept)
+
+
+def test_dense_tail_rows_equal_dense_attention():
+    """Rows in the dense tail keep every candidate, so their sparse output is plain causal
+    attention (no pooled term)."""
+    q, k, v, s = sparse_case(52)
+    N = q.shape[1]
+    out, _ = oracle.sparse(q, k, v, s, 8, 0.1, rules=oracle.KeepRules(dense_tail_rows=16))
+    dense = oracle.dense(q, k[:, :s], v[:, :s], k[:, s:], v[:, s:], s)
+    assert np.max(np.abs(out[0, N - 16:] - dense[0, N - 16:])) <= 1e-12
+    assert np.max(np.abs(out[0, :N - 16] - dense[0, :N - 16])) > 1e-6    # the rest is sparse
