@@ -154,10 +154,28 @@ pf_status pf_sparse_query_sizes(const pf_shape* shape, int32_t start_pos, int32_
  * s_ib - max_c s_ic >= ln(alpha) (alpha = 0 keeps every candidate); the
  * diagonal block ob is always kept.  q [B, C, Hq, d]; k [B, start_pos + C, Hkv, d]
  * (history and chunk contiguous in one cache, strides kh_stride).
- * Requirements: block == 128, 0 <= alpha <= 1, start_pos % 128 == 0.
+ * rules (optional, NULL = the rule above alone): the keep rules of the Metal
+ * port's selection map ("Porting FlashPrefill V2 to Apple silicon for faster
+ * prefill", section "At 16k, only 28% of visible blocks run in full"), applied
+ * in this order:
+ *   sink_tokens      candidates holding keys j < sink_tokens are kept;
+ *   local_blocks     the candidates ob - local_blocks .. ob - 1 are kept;
+ *   dense_tail_rows  rows at p >= start_pos + C - dense_tail_rows keep every
+ *                    candidate;
+ *   row_group        1, or 32: the rows of each aligned 32-position query tile
+ *                    share the union of their kept blocks;
+ *   share_kv_group   0, or 1: the query heads of one KV head share the union
+ *                    of their kept blocks (row by row).
+ * Requirements: block == 128, 0 <= alpha <= 1, start_pos % 128 == 0; rule
+ * counts >= 0 (PF_EINVAL); row_group in {1, 32} (PF_EUNSUPPORTED).
  */
+typedef struct {
+  int32_t sink_tokens, local_blocks, dense_tail_rows, row_group, share_kv_group;
+} pf_keep_rules;
+
 pf_status pf_block_index(const pf_shape* shape, const void* q, const void* k, int32_t start_pos,
-                         int32_t block, float alpha, const pf_sel* sel, void* stream);
+                         int32_t block, float alpha, const pf_keep_rules* rules,
+                         const pf_sel* sel, void* stream);
 
 /*
  * Block-sparse attention with pooled correction.  Row i (p = start_pos + i),

@@ -48,6 +48,14 @@ enum {
 };
 enum { R_PROD = 1, R_MMA = 2, R_ROW = 3 };
 
+// Bits of word w (blocks 32w .. 32w + 31) for the blocks lo <= b < hi.
+__device__ __forceinline__ uint32_t range_bits(int w, int lo, int hi) {
+  const int a0 = max(lo - 32 * w, 0), a1 = min(hi - 32 * w, 32);
+  if (a1 <= a0) return 0u;
+  const uint32_t below_a1 = (a1 == 32) ? 0xFFFFFFFFu : ((1u << a1) - 1u);
+  return below_a1 & ~((1u << a0) - 1u);
+}
+
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, long long timeout,
                                          volatile int* abort_flag, unsigned* status,
                                          unsigned where) {
@@ -206,6 +214,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     const uint32_t dbit = 1u << (ob & 31);
     float smax = -INFINITY;
     bool ok = true;
+    const bool tail_row = a.s + row >= a.tail_from;  // dense-tail rule: keep every candidate
     for (int t = 0; t < nsteps; ++t) {
       const int u = t % 2, pass = t / np, pt = t % np;
       ok = wait_all(XB(I_SF + 2 * sl + u), (uint32_t)(t / 2) & 1u, a.timeout, abort_flag, a.status,
@@ -232,6 +241,14 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
             if (c < lim && (__uint_as_float(xr[c]) - smax) * a.scale >= a.log_alpha) word |= 1u << i;
           }
           const int w = pt * 4 + q;
+          // keep rules on this word's candidates (blocks below ob): sinks, the local
+          // window, the dense tail; then the 32-row query tile's union (a warp's rows are
+          // one aligned 32-position tile)
+          const uint32_t rule = tail_row ? 0xFFFFFFFFu
+                                         : (range_bits(w, 0, a.sink_blocks) |
+                                            range_bits(w, ob - a.local_blocks, ob));
+          word |= rule & range_bits(w, 0, ob);
+          if (a.row_group32) word = __reduce_or_sync(0xffffffffu, valid ? word : 0u);
           if (w == dword) word |= dbit;
           if (w < a.words) {
             if (valid) bits[w] = word;
@@ -285,6 +302,65 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
 }
 
 }  // namespace
+
+// One CTA per (query tile, batch x KV head), thread r = tile row r: the row's words are
+// ORed over the KV head's G query heads and written back to each; the tile's union is
+// then compacted into every head's tile list (ascending).
+__global__ void __launch_bounds__(128) share_group_kernel(const IndexArgs a) {
+  __shared__ uint32_t un[kMaxWords];
+  const int qt = blockIdx.x;
+  const int b = blockIdx.y / a.Hkv, g = blockIdx.y % a.Hkv;
+  const int r = threadIdx.x, lane = r & 31;
+  const int row = qt * kTile + r;
+  const bool valid = row < a.C;
+  for (int w = r; w < kMaxWords; w += blockDim.x) un[w] = 0u;
+  __syncthreads();
+  for (int w = 0; w < a.words; ++w) {
+    uint32_t acc = 0u;
+    if (valid) {
+      for (int j = 0; j < a.G; ++j)
+        acc |= a.row_bits[((long long)(b * a.Hq + g * a.G + j) * a.C + row) * a.words + w];
+      for (int j = 0; j < a.G; ++j)
+        a.row_bits[((long long)(b * a.Hq + g * a.G + j) * a.C + row) * a.words + w] = acc;
+    }
+    const uint32_t uw = __reduce_or_sync(0xffffffffu, acc);
+    if (lane == 0 && uw) atomicOr(&un[w], uw);
+  }
+  __syncthreads();
+  if (r < 32) {
+    int base = 0;
+    for (int w0 = 0; w0 < a.words; w0 += 32) {
+      const int w = w0 + lane;
+      const uint32_t bw = (w < a.words) ? un[w] : 0u;
+      const int cnt = __popc(bw);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      for (int j = 0; j < a.G; ++j) {
+        int32_t* list = a.tile_list + ((long long)(b * a.Hq + g * a.G + j) * a.n_qt + qt) * a.nblk;
+        int pos = base + incl - cnt;
+        uint32_t rb = bw;
+        while (rb) {
+          const int i = __ffs(rb) - 1;
+          rb &= rb - 1u;
+          list[pos++] = w * 32 + i;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0)
+      for (int j = 0; j < a.G; ++j) a.tile_cnt[(long long)(b * a.Hq + g * a.G + j) * a.n_qt + qt] = base;
+  }
+}
+
+cudaError_t launch_share_group(const IndexArgs& a, cudaStream_t st) {
+  share_group_kernel<<<dim3(a.n_qt, a.B * a.Hkv), 128, 0, st>>>(a);
+  ++t_launches;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st) {
   static bool configured = false;

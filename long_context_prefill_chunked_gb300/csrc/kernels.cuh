@@ -89,6 +89,11 @@ struct IndexArgs {
   int slots, n_hp;       // query heads per CTA (1 or 2) and head groups per batch
   float scale;
   float log_alpha;       // ln(alpha); -inf when alpha == 0
+  // keep rules (all zero = the alpha rule alone)
+  int sink_blocks;       // candidates b < sink_blocks are kept
+  int local_blocks;      // candidates b >= ob - local_blocks are kept
+  int tail_from;         // rows at positions p >= tail_from keep every candidate
+  int row_group32;       // 1: the 32 rows of a warp share the union of their kept blocks
   uint32_t* row_bits;
   int32_t* tile_list;
   int32_t* tile_cnt;
@@ -99,6 +104,9 @@ struct IndexMaps {
   CUtensorMap q, hi, lo;
 };
 cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st);
+// Shared selection of a KV group: row bits ORed over the group's G query heads, written
+// back to each, and each head's tile lists rebuilt from them.
+cudaError_t launch_share_group(const IndexArgs& a, cudaStream_t st);
 
 extern thread_local long long t_launches;
 

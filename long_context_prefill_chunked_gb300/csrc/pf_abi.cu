@@ -408,12 +408,20 @@ pf_status check_sparse(const pf_shape* sh, int32_t start_pos, int32_t block, lon
 }  // namespace
 
 pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32_t start_pos,
-                         int32_t block, float alpha, const pf_sel* sel, void* stream) {
+                         int32_t block, float alpha, const pf_keep_rules* rules,
+                         const pf_sel* sel, void* stream) {
   long long ks[3], qs[3];
   pf_sparse_sizes z;
   pf_status rc = check_sparse(sh, start_pos, block, ks, qs, &z);
   if (rc != PF_OK) return rc;
   if (!(alpha >= 0.f && alpha <= 1.f)) return fail(PF_EUNSUPPORTED, "alpha %g outside [0, 1]", alpha);
+  pf_keep_rules kr{0, 0, 0, 1, 0};
+  if (rules != nullptr) kr = *rules;
+  if (kr.sink_tokens < 0 || kr.local_blocks < 0 || kr.dense_tail_rows < 0)
+    return fail(PF_EINVAL, "keep-rule counts must be >= 0");
+  if (kr.row_group != 1 && kr.row_group != 32)
+    return fail(PF_EUNSUPPORTED, "row_group %d (supported: 1, 32)", kr.row_group);
+  if (kr.share_kv_group != 0 && kr.share_kv_group != 1) return fail(PF_EINVAL, "share_kv_group must be 0 or 1");
   if (q == nullptr || k == nullptr || sel == nullptr || sel->row_bits == nullptr ||
       sel->tile_list == nullptr || sel->tile_cnt == nullptr || sel->kbar == nullptr)
     return fail(PF_EINVAL, "q, k and every pf_sel buffer must be non-NULL");
@@ -458,6 +466,10 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
   ia.n_hp = sh->Hq / ia.slots;
   ia.scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)d);
   ia.log_alpha = alpha > 0.f ? logf(alpha) : -INFINITY;
+  ia.sink_blocks = (int)(((long long)kr.sink_tokens + kTile - 1) / kTile);
+  ia.local_blocks = kr.local_blocks;
+  ia.tail_from = (int)((long long)T - kr.dense_tail_rows);
+  ia.row_group32 = kr.row_group == 32 ? 1 : 0;
   ia.row_bits = sel->row_bits;
   ia.tile_list = sel->tile_list;
   ia.tile_cnt = sel->tile_cnt;
@@ -474,6 +486,8 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
                      "kbar lo")) != PF_OK)
     return rc;
   if ((e = launch_index(maps, ia, st)) != cudaSuccess) return cuda_fail(e, "index launch");
+  if (kr.share_kv_group && ia.G > 1 && (e = launch_share_group(ia, st)) != cudaSuccess)
+    return cuda_fail(e, "shared-selection launch");
   return PF_OK;
 }
 

@@ -55,6 +55,16 @@ class Sel(ctypes.Structure):
                 ("tile_cnt", ctypes.c_void_p), ("kbar", ctypes.c_void_p)]
 
 
+class KeepRules(ctypes.Structure):
+    """pf_keep_rules: sinks (tokens), local window (blocks), dense tail (rows), row_group
+    (1 or 32), share_kv_group (0 or 1)."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("sink_tokens", "local_blocks", "dense_tail_rows",
+                                              "row_group", "share_kv_group")]
+
+    def __init__(self, sink_tokens=0, local_blocks=0, dense_tail_rows=0, row_group=1, share_kv_group=0):
+        super().__init__(sink_tokens, local_blocks, dense_tail_rows, row_group, int(share_kv_group))
+
+
 class SparseSizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("nblk", "nqt", "words", "row_bits_elems", "tile_list_elems",
                                               "tile_cnt_elems", "kbar_elems", "pooled_bytes")]
@@ -74,7 +84,7 @@ def load() -> ctypes.CDLL:
     V, I32, I64, F, P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.POINTER
     lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V, V, I64, V]
     lib.pf_dense_workspace_bytes.argtypes = [P(Shape), P(I64)]
-    lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(Sel), V]
+    lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(KeepRules), P(Sel), V]
     lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V, V]
     lib.pf_sparse_query_sizes.argtypes = [P(Shape), I32, I32, P(SparseSizes)]
     lib.pf_stream_status.argtypes = [V]
@@ -280,8 +290,9 @@ def alloc_selection(q, k, start_pos, block=128) -> Selection:
                      torch.empty((2, B, Hkv, z.nblk, d), dtype=torch.float32, device=dev))
 
 
-def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stream=None) -> Selection:
-    """Pooled block selection (pf_block_index)."""
+def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stream=None,
+                rules: KeepRules = None) -> Selection:
+    """Pooled block selection (pf_block_index); rules: optional KeepRules."""
     lib = load()
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q must be [B, C, Hq, d] and k [B, start_pos + C, Hkv, d]")
@@ -294,7 +305,8 @@ def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stre
     sh.kh_stride = _bth(k)
     cs = sel.c_struct()
     _check(lib.pf_block_index(ctypes.byref(sh), _ptr(q), _ptr(k), int(start_pos), int(block),
-                              float(alpha), ctypes.byref(cs), _stream(stream)))
+                              float(alpha), ctypes.byref(rules) if rules is not None else None,
+                              ctypes.byref(cs), _stream(stream)))
     return sel
 
 

@@ -85,10 +85,16 @@ def test_dense_rejects_bad_arguments(lib):
 def test_sparse_rejects_bad_arguments(lib):
     sel = pf.Sel(0x100000, 0x100000, 0x100000, 0x100000)
     sh = shape()
-    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 64, 0.1, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
-    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, 1.5, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
-    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, -0.1, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
-    assert lib.pf_block_index(ctypes.byref(sh), None, FAKE, 0, 128, 0.1, ctypes.byref(sel), None) == pf.PF_EINVAL
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 64, 0.1, None, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, 1.5, None, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, -0.1, None, ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
+    assert lib.pf_block_index(ctypes.byref(sh), None, FAKE, 0, 128, 0.1, None, ctypes.byref(sel), None) == pf.PF_EINVAL
+    bad_group = pf.KeepRules(row_group=16)
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, 0.1, ctypes.byref(bad_group),
+                              ctypes.byref(sel), None) == pf.PF_EUNSUPPORTED
+    bad_count = pf.KeepRules(sink_tokens=-1)
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 0, 128, 0.1, ctypes.byref(bad_count),
+                              ctypes.byref(sel), None) == pf.PF_EINVAL
     assert lib.pf_attn_sparse(ctypes.byref(sh), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), None, FAKE, None, None) == pf.PF_EINVAL
     long = shape(C=300000)
     assert lib.pf_attn_sparse(ctypes.byref(long), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), FAKE, FAKE, None, None) == pf.PF_EUNSUPPORTED

@@ -7,6 +7,7 @@ import torch
 import oracle
 import prefill_inputs as pi
 from gpu_util import MAX_ABS, assert_close, dev, errors, sample_rows
+from long_context_prefill_chunked_gb300 import pf
 
 pytestmark = pytest.mark.gpu
 
@@ -189,3 +190,37 @@ def test_sparse_lse_matches_oracle(small):
         pooled_max = np.abs(np.where(np.isfinite(osel.scores), osel.scores, 0.0)).max()
         tol = 1e-4 if alpha == 0.0 else 1e-4 + 2.0 ** -9 * pooled_max
         assert np.max(np.abs(got - rlse)[ok]) <= tol, (alpha, np.max(np.abs(got - rlse)[ok]), tol)
+
+
+# --------------------------------------------------------------------------- keep rules
+RULES = [
+    ("sinks-window", dict(sink_tokens=256, local_blocks=1)),
+    ("tail", dict(dense_tail_rows=64)),
+    ("row32", dict(row_group=32)),
+    ("shared", dict(share_kv_group=1)),
+    ("all", dict(sink_tokens=256, local_blocks=2, dense_tail_rows=64, row_group=32, share_kv_group=1)),
+]
+
+
+@pytest.mark.parametrize("name,kw", RULES)
+def test_keep_rules_selection_and_output(small, name, kw):
+    """Selection under the Metal port's keep rules: row bits and tile lists bit-exact with
+    the oracle outside the near band (propagated through the group unions), outputs within
+    tolerance."""
+    w = small
+    s, C = 1024, 1024
+    q = dev(w.q[:, s:s + C], w.dtype)
+    k = dev(w.k[:, :s + C], w.dtype)
+    v = dev(w.v[:, :s + C], w.dtype)
+    sel = pfx.block_index(q, k, s, 128, 0.1, rules=pf.KeepRules(**kw))
+    out = pfx.attn_sparse(q, k, v, s, sel)
+    pfx.stream_status()
+    okw = dict(kw)
+    okw["share_kv_group"] = bool(okw.get("share_kv_group", 0))
+    ref, osel = oracle.sparse(w.f64(w.q[:, s:s + C]), w.f64(w.k[:, :s + C]), w.f64(w.v[:, :s + C]), s, 128,
+                              0.1, rules=oracle.KeepRules(**okw))
+    check_selection(sel, osel, np.arange(C))
+    check_tile_lists(sel, osel, C)
+    ok = ~osel.near
+    e = np.abs(out.cpu().double().numpy() - ref)[ok]
+    assert e.max() <= MAX_ABS and e.mean() <= 5e-4, (e.max(), e.mean())
