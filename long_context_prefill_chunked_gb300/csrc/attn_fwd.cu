@@ -188,7 +188,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     fence_mbar_init();
   }
   if (MODE == MODE_SPARSE && warp == 8) {
-    // Union of the slots' kept-block lists, ascending, via a bitmap.
+    // Union of the slots' kept-block lists, ascending, via a bitmap.  Only earlier
+    // blocks (< ob) are taken from the lists and the diagonal block ob is always set,
+    // so ob is the union's last block whatever the lists hold.  The count goes through
+    // shared memory: every role reads it after its setmaxnreg (a value held in a
+    // register across that point may be lost).
     uint32_t* bm = reinterpret_cast<uint32_t*>(smem + SM_BM);
     const long long t0 = (long long)(b * a.Hq + h0) * a.n_qt + qt;
     const int32_t* l0 = a.tile_list + t0 * a.nblk;
@@ -197,13 +201,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int32_t* l1 = l0 + (long long)a.n_qt * a.nblk;
     for (int w = lane; w < a.words; w += 32) bm[w] = 0u;
     __syncwarp();
-    for (int i = lane; i < c0; i += 32) {
-      const int kb = l0[i];
-      if (kb >= 0 && kb < a.nblk) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
-    }
-    for (int i = lane; i < c1; i += 32) {
-      const int kb = l1[i];
-      if (kb >= 0 && kb < a.nblk) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
+    if (lane == 0) atomicOr(&bm[ob >> 5], 1u << (ob & 31));
+    for (int i = lane; i < c0 + c1; i += 32) {
+      const int kb = i < c0 ? l0[i] : l1[i - c0];
+      if (kb >= 0 && kb < ob) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
     }
     __syncwarp();
     int cnt = 0;
