@@ -601,24 +601,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (a.lse != nullptr && valid)
         a.lse[((long long)b * a.Hq + h) * a.C + row] = (mm + __log2f(ll)) * 0.6931471805599453f;
     };
-    if (split < 0 && MODE == MODE_SPARSE) {
-      // Sparse units are short (tens of tiles): direct row stores keep this mode's loop
-      // registers (a staged tile store measured slower here).
-      if (ok) {
-        tc_fence_after();
-        write_lse(m, l);
-        const float inv = 1.f / l;
-        for (int c0 = 0; c0 < a.d; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(t_o + c0, o);
-          tmem_wait_ld();
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv;
-          if (valid) store_out32(a, obase + c0, v);
-        }
-      }
-    } else if (split < 0) {
+    if (split < 0) {
       // Rows are staged in shared memory (the Q and K stages are free once every MMA is
       // done: slot s uses [64 KB * s, 64 KB * (s + 1))) as 128-byte boxes, 16-byte chunks
       // swizzled the way the tile store reads them, then one thread per head stores the
