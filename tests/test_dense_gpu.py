@@ -236,3 +236,30 @@ def test_lse_matches_oracle(case):
     assert_close(out, ref, "lse case " + case)
     got = lse.cpu().double().numpy().transpose(0, 2, 1)          # [B, C, Hq]
     assert np.max(np.abs(got - rlse)) <= LSE_TOL, np.max(np.abs(got - rlse))
+
+
+# --------------------------------------------------------------------------- the bench's launches
+@pytest.mark.slow
+def test_config4_dense_chunked_as_benchmarked():
+    """The 32K prompt as bench.py runs it: 8 chunks of 4096 causal rows over the previous
+    chunks' K/V, chunk outputs written into one [1, 32768, 32, 128] tensor, K/V emitted into a
+    head-major cache, the tail-split workspace on.  Sampled rows of every chunk against the
+    oracle; the cache must be a bit copy."""
+    w = pi.config(4)
+    N, CH = w.N, 4096
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    Q, K, V = to(w.q), to(w.k), to(w.v)
+    out = torch.empty((1, N, 32, 128), dtype=torch.float32, device="cuda")
+    ck = torch.empty((1, 8, N, 128), dtype=torch.bfloat16, device="cuda")
+    cv = torch.empty_like(ck)
+    for s in range(0, N, CH):
+        pfx.attn_dense(Q[:, s:s + CH], K[:, :s], V[:, :s], K[:, s:s + CH], V[:, s:s + CH], s,
+                       out=out[:, s:s + CH], out_k=ck[:, :, s:s + CH], out_v=cv[:, :, s:s + CH])
+    pfx.stream_status()
+    assert torch.equal(ck.transpose(1, 2).contiguous(), K) and torch.equal(cv.transpose(1, 2).contiguous(), V)
+    q64, k64, v64 = w.f64(w.q), w.f64(w.k), w.f64(w.v)
+    for ci, s in enumerate(range(0, N, CH)):
+        rows = sample_rows(CH, 48, 400 + ci)
+        ref = oracle.dense(q64[:, s:s + CH], k64[:, :s], v64[:, :s], k64[:, s:s + CH], v64[:, s:s + CH], s,
+                           rows=rows)
+        assert_close(out[:, s + rows], ref, "32K chunk at %d" % s)
