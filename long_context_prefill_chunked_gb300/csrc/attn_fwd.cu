@@ -196,14 +196,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint32_t* bm = reinterpret_cast<uint32_t*>(smem + SM_BM);
     const long long t0 = (long long)(b * a.Hq + h0) * a.n_qt + qt;
     const int32_t* l0 = a.tile_list + t0 * a.nblk;
-    const int c0 = min(max(a.tile_cnt[t0], 0), a.nblk);
-    const int c1 = (a.slots == 2) ? min(max(a.tile_cnt[t0 + a.n_qt], 0), a.nblk) : 0;
     const int32_t* l1 = l0 + (long long)a.n_qt * a.nblk;
+    // the counts and the first 64 entries of both lists in one round trip (every list row
+    // holds nblk entries, so the reads stay in bounds; entries past a count are ignored)
+    const int raw0 = a.tile_cnt[t0];
+    const int raw1 = (a.slots == 2) ? a.tile_cnt[t0 + a.n_qt] : 0;
+    int e0[2], e1[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = lane + 32 * u;
+      e0[u] = i < a.nblk ? l0[i] : -1;
+      e1[u] = (a.slots == 2 && i < a.nblk) ? l1[i] : -1;
+    }
+    const int c0 = min(max(raw0, 0), a.nblk);
+    const int c1 = min(max(raw1, 0), a.nblk);
     for (int w = lane; w < a.words; w += 32) bm[w] = 0u;
     __syncwarp();
     if (lane == 0) atomicOr(&bm[ob >> 5], 1u << (ob & 31));
-    for (int i = lane; i < c0 + c1; i += 32) {
-      const int kb = i < c0 ? l0[i] : l1[i - c0];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = lane + 32 * u;
+      if (i < c0 && e0[u] >= 0 && e0[u] < ob) atomicOr(&bm[e0[u] >> 5], 1u << (e0[u] & 31));
+      if (i < c1 && e1[u] >= 0 && e1[u] < ob) atomicOr(&bm[e1[u] >> 5], 1u << (e1[u] & 31));
+    }
+    for (int i = 64 + lane; i < c0; i += 32) {
+      const int kb = l0[i];
+      if (kb >= 0 && kb < ob) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
+    }
+    for (int i = 64 + lane; i < c1; i += 32) {
+      const int kb = l1[i];
       if (kb >= 0 && kb < ob) atomicOr(&bm[kb >> 5], 1u << (kb & 31));
     }
     __syncwarp();
