@@ -10,11 +10,15 @@
 // section "Compute the peaks, summarize the rest".
 //
 // One CTA = one work unit = (batch b, query tile of 128 rows, `slots` query
-// heads of the same KV group).  The slots share every K/V tile (GQA): one TMA
-// load feeds both heads' MMAs.
+// heads of the same KV group), or one part of a unit's key range when the
+// dense tail split is on (the last part to finish merges the parts' partial
+// results).  The slots share every K/V tile (GQA): one TMA load feeds both
+// heads' MMAs.  Units run heaviest first (sparse: through a longest-first
+// permutation).
 //   warps 0-3  softmax for slot 0 (thread t owns query row t = TMEM lane t)
 //   warps 4-7  softmax for slot 1
-//   warp  8    TMA producer (Q once, then K and V tiles through two 2-stage rings)
+//   warp  8    TMA producer (Q once, then K tiles through a 2-stage ring and V
+//              tiles through a 3-stage ring)
 //   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
 //   warps 10-11 V converters: for bf16 inputs they rewrite each landed V tile
 //              in place as fp16, so that P * V runs as an fp16 MMA (P carries
@@ -27,7 +31,12 @@
 // S(slot1, j+1); each softmax group works on its tile while the tensor core
 // runs the other slot's pair.  K and V have separate rings: a K stage is freed
 // as soon as both S MMAs that read it are done, so K tile j+1 is in flight
-// while tile j's softmax runs.
+// while tile j's softmax runs.  The epilogue stages O / l in the freed Q and K
+// stages and writes it with TMA tile stores (optionally also the row's
+// log-sum-exp).
+// Values computed before the warp-role split reach the roles through shared
+// memory or are recomputed: the producer warpgroup's setmaxnreg.dec may drop
+// registers above its new limit.
 #include <cuda_fp16.h>
 #include <math.h>
 
