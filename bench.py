@@ -268,7 +268,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse", "sparse-128k-chunk"],
@@ -314,13 +314,14 @@ def main():
     def mk():
         return torch.cuda.Event(enable_timing=True)
 
-    def step(q, k, v, ev=None):
+    def step(q, k, v, ev=None, outs=None):
+        o_d, o_s, c_k, c_v = outs if outs is not None else (out_d, out_s, cache_k, cache_v)
         for i, s in enumerate(starts):
             if ev is not None:
                 ev["dense"][i][0].record(stream)
             pfx.attn_dense(q[:, s:s + CHUNK], k[:, :s], v[:, :s], k[:, s:s + CHUNK], v[:, s:s + CHUNK], s,
-                           out=out_d[:, s:s + CHUNK], out_k=cache_k[:, :, s:s + CHUNK],
-                           out_v=cache_v[:, :, s:s + CHUNK], stream=stream)
+                           out=o_d[:, s:s + CHUNK], out_k=c_k[:, :, s:s + CHUNK],
+                           out_v=c_v[:, :, s:s + CHUNK], stream=stream)
             if ev is not None:
                 ev["dense"][i][1].record(stream)
         if ev is not None:
@@ -329,7 +330,7 @@ def main():
         if ev is not None:
             ev["index"][1].record(stream)
             ev["sparse"][0].record(stream)
-        pfx.attn_sparse(q, k, v, 0, sel, block=BLOCK, pooled=pooled, out=out_s, stream=stream)
+        pfx.attn_sparse(q, k, v, 0, sel, block=BLOCK, pooled=pooled, out=o_s, stream=stream)
         if ev is not None:
             ev["sparse"][1].record(stream)
 
@@ -390,38 +391,60 @@ def main():
     cand = HQ * sum(range(n_qt))
     skip_tiles = 1.0 - (tc - 1).sum() / cand
 
-    # e2e: host buffers in, host buffers out, through the same public API
+    # e2e: host buffers in, host buffers out, through the same public API.  Pipelined as a
+    # serving loop would run it: two buffer sets, the next step's H2D and the previous step's
+    # D2H on their own streams while this step computes; the window runs from the first H2D
+    # to the last D2H.
     hq = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
     hk = torch.from_numpy(w.k.view(np.int16)).view(torch.bfloat16).pin_memory()
     hv = torch.from_numpy(w.v.view(np.int16)).view(torch.bfloat16).pin_memory()
-    ho_d = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
-    ho_s = torch.empty(out_s.shape, dtype=out_s.dtype).pin_memory()
-    hck = torch.empty(cache_k.shape, dtype=cache_k.dtype).pin_memory()
-    hcv = torch.empty(cache_v.shape, dtype=cache_v.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
+    sets = []
+    for b in range(2):
+        dins = (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V))
+        douts = (out_d, out_s, cache_k, cache_v) if b == 0 else tuple(torch.empty_like(t) for t in
+                                                                         (out_d, out_s, cache_k, cache_v))
+        houts = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in douts)
+        sets.append({"in": dins, "out": douts, "host": houts, "in_ready": torch.cuda.Event(),
+                     "comp_done": torch.cuda.Event(), "out_done": torch.cuda.Event(), "used": False})
 
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        step(dq, dk, dv)
-        ho_d.copy_(out_d, non_blocking=True)
-        ho_s.copy_(out_s, non_blocking=True)
-        hck.copy_(cache_k, non_blocking=True)
-        hcv.copy_(cache_v, non_blocking=True)
+    def e2e_step(i):
+        bs = sets[i % 2]
+        with torch.cuda.stream(h2d_stream):
+            if bs["used"]:
+                h2d_stream.wait_event(bs["comp_done"])      # step i-2 has read these inputs
+            for d, h in zip(bs["in"], (hq, hk, hv)):
+                d.copy_(h, non_blocking=True)
+            bs["in_ready"].record(h2d_stream)
+        stream.wait_event(bs["in_ready"])
+        if bs["used"]:
+            stream.wait_event(bs["out_done"])             # step i-2's outputs are on the host
+        step(*bs["in"], outs=bs["out"])
+        bs["comp_done"].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(bs["comp_done"])
+            for hbuf, d in zip(bs["host"], bs["out"]):
+                hbuf.copy_(d, non_blocking=True)
+            bs["out_done"].record(d2h_stream)
+        bs["used"] = True
 
-    e2e_step()                              # untimed warm-up of the copy path
-    e0, e1 = mk(), mk()
+    for i in range(2):                      # untimed warm-up of both buffer sets
+        e2e_step(i)
     torch.cuda.synchronize(dev)
+    e0, e1 = mk(), mk()
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    h2d_stream.wait_event(e0)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    for bs in sets:
+        stream.wait_event(bs["out_done"])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev, world)
     pfx.stream_status(stream)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
-    d2h = sum(x.numel() * x.element_size() for x in (ho_d, ho_s, hck, hcv))
+    d2h = sum(x.numel() * x.element_size() for x in sets[0]["host"])
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -449,7 +472,9 @@ def main():
                                "chunk's two cache-layout copies)",
                      "peak_source": "%s bf16_tflops (burst)" % peak_src},
         "e2e": {"value": weak_scaling_value(f_dense + f_sparse, e2e_ms, world), "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipelining": "two buffer sets; step i+1's H2D and step i-1's D2H overlap step i on "
+                              "their own streams; window from the first H2D to the last D2H"},
         "gpu_launches": launches,
         "clocks": clk,
     }
