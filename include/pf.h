@@ -125,6 +125,12 @@ pf_status pf_attn_dense(const pf_shape* shape, const void* q, const void* k_hist
  * device (about 20 MB for d = 128 on 152 SMs; independent of the sequence). */
 pf_status pf_dense_workspace_bytes(const pf_shape* shape, int64_t* bytes);
 
+/* Workspace bytes for a call with an explicit mask: the above plus room for the mask packed
+ * to bits (C * ceil((start_pos + C) / 128) * 16 bytes).  With a workspace of this size a mask
+ * whose values are all 0 or <= -10000 (and that keeps a key in every row) is read as bits, the
+ * same result as reading the values; any other mask is read as values. */
+pf_status pf_dense_workspace_bytes_masked(const pf_shape* shape, int32_t start_pos, int64_t* bytes);
+
 /* Block selection produced by pf_block_index and consumed by pf_attn_sparse.
  * nblk = ceil((start_pos + C) / block); nqt = ceil(C / 128); W = ceil(nblk / 32). */
 typedef struct {

@@ -466,9 +466,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bits_row = a.row_bits + ((long long)(b * a.Hq + h) * a.C + row) * a.words;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // binary explicit mask read as bits (one 16-byte word group per row and tile)
+    const uint4* mbits = nullptr;
+    if (MODE == MODE_MASK && a.mask_bits != nullptr && valid && __ldg(a.mask_binary) != 0)
+      mbits = reinterpret_cast<const uint4*>(a.mask_bits + (long long)row * a.mask_words);
+    uint4 nbits = make_uint4(0u, 0u, 0u, 0u);  // the next tile's mask bits, loaded a tile ahead
+    if (MODE == MODE_MASK && mbits != nullptr) nbits = __ldg(mbits + j0);
     BlockWalk walk;
     if (MODE == MODE_SPARSE) walk.init(kept_bm);
     for (int j = 0; j < n_tiles; ++j) {
+      const uint4 bw = nbits;
+      if (MODE == MODE_MASK && mbits != nullptr && j + 1 < n_tiles) nbits = __ldg(mbits + (j0 + j + 1));
       ok = wait_all(BAR(B_SF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
                     (R_SOFT << 8) | (B_SF + sl));
       if (!ok) break;
@@ -483,6 +491,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c > r) x[c] = -INFINITY;
         }
+      } else if (MODE == MODE_MASK && mbits != nullptr) {
+        // bit set = kept (value 0); dropped keys (and keys past T, whose bits are 0) are -inf
+        const uint32_t wq[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (!((wq[q] >> i) & 1u)) x[32 * q + i] = -INFINITY;
       } else if (MODE == MODE_MASK) {
         xs = 1.f;
         const int key0 = (j0 + j) * kTile;
@@ -747,6 +763,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #undef BAR
 }
 
+// One CTA per mask row (rows past 65535 loop): warp-wide loads of 32 consecutive values
+// become one word through a ballot; the row's kept count decides whether a fully dropped row
+// (a plain softmax over the raw scores with values, NaN with bits) forces the value path.
+__global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__ mask, int f16, int C,
+                                                        int T, long long ld, uint32_t* __restrict__ bits,
+                                                        int words, int* binary) {
+  __shared__ int kept_any;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int row = blockIdx.y; row < C; row += gridDim.y) {
+    if (threadIdx.x == 0) kept_any = 0;
+    __syncthreads();
+    bool nonbin = false, any = false;
+    for (int w = warp; w < words; w += blockDim.x / 32) {
+      const int key = w * 32 + lane;
+      bool keep = false;
+      if (key < T) {
+        const long long o = (long long)row * ld + key;
+        const float v = f16 ? __half2float(reinterpret_cast<const __half*>(mask)[o])
+                            : reinterpret_cast<const float*>(mask)[o];
+        keep = v == 0.f;
+        nonbin |= !(v == 0.f || v <= -10000.f);
+      }
+      const uint32_t word = __ballot_sync(0xffffffffu, keep);
+      any |= word != 0u;
+      if (lane == 0) bits[(long long)row * words + w] = word;
+    }
+    if (__any_sync(0xffffffffu, any) && lane == 0) kept_any = 1;
+    if (__any_sync(0xffffffffu, nonbin) && lane == 0) atomicExch(binary, 0);
+    __syncthreads();
+    if (threadIdx.x == 0 && !kept_any) atomicExch(binary, 0);
+    __syncthreads();
+  }
+}
+
 __global__ void kv_relayout_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                    int B, int C, int H, int d, long long s0, long long s1,
                                    long long s2, long long d0, long long d1, long long d2) {
@@ -789,6 +839,14 @@ cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaS
     case MODE_MASK: return launch_mode<MODE_MASK>(maps, a, st);
     default: return launch_mode<MODE_SPARSE>(maps, a, st);
   }
+}
+
+cudaError_t launch_mask_pack(const void* mask, int f16, int C, int T, long long ld, uint32_t* bits,
+                             int words, int* binary, cudaStream_t st) {
+  const dim3 grid(1, C < 65535 ? C : 65535);
+  mask_pack_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, binary);
+  ++t_launches;
+  return cudaGetLastError();
 }
 
 cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, int d,

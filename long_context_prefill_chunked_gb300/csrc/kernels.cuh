@@ -26,6 +26,11 @@ struct AttnArgs {
   int mask_f16;         // 1 = fp16 mask, 0 = fp32
   int mask_vec;         // rows 16-byte aligned: vector loads allowed
   long long mask_ld;    // elements between mask rows
+  // the same mask packed to bits when every value is 0 or <= -10000 (bit set = kept);
+  // used only while *mask_binary != 0 (the packing pass clears it otherwise)
+  const uint32_t* mask_bits;  // [C][mask_words], rows padded to a multiple of 4 words
+  int mask_words;
+  const int* mask_binary;
   // output
   void* out;
   float* lse;           // [B, Hq, C] log of each row's softmax denominator, or null
@@ -57,6 +62,10 @@ struct AttnMaps {
 };
 
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaStream_t st);
+// Packs an additive mask [C, T] (row stride ld) into bits [C][words] (kept iff the value is 0)
+// and clears *binary when a value is neither 0 nor <= -10000 or a row keeps no key.
+cudaError_t launch_mask_pack(const void* mask, int f16, int C, int T, long long ld, uint32_t* bits,
+                             int words, int* binary, cudaStream_t st);
 
 // bit copy of the chunk's K (or V) into the cache layout
 cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, int d,

@@ -263,6 +263,22 @@ pf_status pf_stream_status(void* stream) {
               w[1] >> 8, w[1] & 0xFFu);
 }
 
+long long mask_words_of(long long T) { return (T + kTile - 1) / kTile * 4; }
+
+long long dense_masked_workspace_bytes(int d, int sms, int C, long long T) {
+  return dense_workspace_bytes(d, sms) + 256 + (long long)C * mask_words_of(T) * 4;
+}
+
+pf_status pf_dense_workspace_bytes_masked(const pf_shape* sh, int32_t start_pos, int64_t* bytes) {
+  if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
+  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  if (sh->C < 1 || start_pos < 0) return fail(PF_EINVAL, "C >= 1 and start_pos >= 0 required");
+  const int P = sm_count();
+  if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
+  *bytes = dense_masked_workspace_bytes(sh->d, P, sh->C, (long long)start_pos + sh->C);
+  return PF_OK;
+}
+
 pf_status pf_dense_workspace_bytes(const pf_shape* sh, int64_t* bytes) {
   if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
   if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
@@ -353,6 +369,21 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   plan_split(a, mode, workspace);
+  if (mode == MODE_MASK && workspace != nullptr &&
+      workspace_bytes >= dense_masked_workspace_bytes(d, sm_count(), C, (long long)s + C)) {
+    // binary masks (0 / <= -10000) are read as bits; the packing pass clears the flag and the
+    // kernels keep the value path when the mask is not binary
+    char* base = static_cast<char*>(workspace) + dense_workspace_bytes(d, sm_count());
+    int* flag = reinterpret_cast<int*>(base);
+    uint32_t* bits = reinterpret_cast<uint32_t*>(base + 256);
+    const int words = (int)mask_words_of((long long)s + C);
+    if ((e = cudaMemsetAsync(flag, 1, sizeof(int), st)) != cudaSuccess) return cuda_fail(e, "mask flag");
+    if ((e = launch_mask_pack(mask, a.mask_f16, C, s + C, a.mask_ld, bits, words, flag, st)) != cudaSuccess)
+      return cuda_fail(e, "mask packing launch");
+    a.mask_bits = bits;
+    a.mask_words = words;
+    a.mask_binary = flag;
+  }
   if (a.split_k > 1) {
     const int n_split = a.n_qt * a.n_hp * a.B - a.n_whole;
     if ((e = cudaMemsetAsync(a.ws_cnt, 0, sizeof(int) * n_split, st)) != cudaSuccess)

@@ -27,7 +27,8 @@ PF_F16, PF_BF16, PF_F32 = range(3)
 STATUS_NAMES = {0: "PF_OK", 1: "PF_EINVAL", 2: "PF_EUNSUPPORTED", 3: "PF_ECUDA", 4: "PF_ETIMEOUT",
                 5: "PF_ERANGE"}
 
-EXPORTS = ["pf_attn_dense", "pf_dense_workspace_bytes", "pf_block_index", "pf_attn_sparse",
+EXPORTS = ["pf_attn_dense", "pf_dense_workspace_bytes", "pf_dense_workspace_bytes_masked",
+           "pf_block_index", "pf_attn_sparse",
            "pf_sparse_query_sizes",
            "pf_stream_status", "pf_set_wait_timeout", "pf_set_debug_withhold", "pf_launch_count",
            "pf_last_error", "pf_version"]
@@ -84,6 +85,7 @@ def load() -> ctypes.CDLL:
     V, I32, I64, F, P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.POINTER
     lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V, V, I64, V]
     lib.pf_dense_workspace_bytes.argtypes = [P(Shape), P(I64)]
+    lib.pf_dense_workspace_bytes_masked.argtypes = [P(Shape), I32, P(I64)]
     lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(KeepRules), P(Sel), V]
     lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V, V]
     lib.pf_sparse_query_sizes.argtypes = [P(Shape), I32, I32, P(SparseSizes)]
@@ -96,7 +98,8 @@ def load() -> ctypes.CDLL:
     lib.pf_launch_count.restype = I64
     lib.pf_last_error.restype = ctypes.c_char_p
     lib.pf_version.restype = ctypes.c_char_p
-    for name in ("pf_attn_dense", "pf_dense_workspace_bytes", "pf_block_index", "pf_attn_sparse",
+    for name in ("pf_attn_dense", "pf_dense_workspace_bytes", "pf_dense_workspace_bytes_masked",
+                 "pf_block_index", "pf_attn_sparse",
                  "pf_sparse_query_sizes", "pf_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -175,18 +178,24 @@ def make_shape(q, k_like, out_dtype, scale=0.0) -> Shape:
 _WORKSPACES = {}
 
 
-def dense_workspace(q, stream=None) -> torch.Tensor:
-    """The pf_attn_dense tail-split workspace for q's head dim, one per (device, stream) so
-    that calls on different streams never share one."""
+def dense_workspace(q, stream=None, masked_start_pos=None) -> torch.Tensor:
+    """The pf_attn_dense workspace (tail split; with masked_start_pos, also the packed bits of
+    an explicit mask) for q, one per (device, stream) so that calls on different streams never
+    share one."""
     lib = load()
     sh = Shape()
     sh.d = q.shape[-1]
+    sh.C = q.shape[1]
     n = ctypes.c_int64(0)
     with torch.cuda.device(q.device):
-        _check(lib.pf_dense_workspace_bytes(ctypes.byref(sh), ctypes.byref(n)))
-    key = (q.device, _stream(stream).value, int(n.value))
+        if masked_start_pos is None:
+            _check(lib.pf_dense_workspace_bytes(ctypes.byref(sh), ctypes.byref(n)))
+        else:
+            _check(lib.pf_dense_workspace_bytes_masked(ctypes.byref(sh), int(masked_start_pos),
+                                                       ctypes.byref(n)))
+    key = (q.device, _stream(stream).value)
     ws = _WORKSPACES.get(key)
-    if ws is None:
+    if ws is None or ws.numel() < int(n.value):
         ws = torch.empty((int(n.value),), dtype=torch.uint8, device=q.device)
         _WORKSPACES[key] = ws
     return ws
@@ -221,7 +230,7 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
         _expect(mask, (C, start_pos + C), "mask", dev)
     _expect_lse(lse, B, Hq, C, dev)
     if workspace is True:
-        workspace = dense_workspace(q, stream)
+        workspace = dense_workspace(q, stream, None if mask is None else start_pos)
     elif workspace is False:
         workspace = None
     if workspace is not None and workspace.device != dev:
