@@ -126,9 +126,12 @@ pf_status pf_attn_dense(const pf_shape* shape, const void* q, const void* k_hist
 pf_status pf_dense_workspace_bytes(const pf_shape* shape, int64_t* bytes);
 
 /* Workspace bytes for a call with an explicit mask: the above plus room for the mask packed
- * to bits (C * ceil((start_pos + C) / 128) * 16 bytes).  With a workspace of this size a mask
- * whose values are all 0 or <= -10000 (and that keeps a key in every row) is read as bits, the
- * same result as reading the values; any other mask is read as values. */
+ * to bits (C * ceil((start_pos + C) / 128) * 16 bytes) and, per 128-row query tile, a bitmap
+ * of the 128-key tiles it keeps.  With a workspace of this size a mask whose values are all 0
+ * or <= -10000 (and that keeps a key in every row) is read as bits, the same result as reading
+ * the values, and a query tile skips every key tile that none of its rows keeps (when
+ * start_pos + C <= 262144; longer calls visit every key tile); any other mask is read as
+ * values. */
 pf_status pf_dense_workspace_bytes_masked(const pf_shape* shape, int32_t start_pos, int64_t* bytes);
 
 /* Block selection produced by pf_block_index and consumed by pf_attn_sparse.

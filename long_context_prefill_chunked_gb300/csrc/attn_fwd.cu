@@ -34,6 +34,9 @@
 // while tile j's softmax runs.  The epilogue stages O / l in the freed Q and K
 // stages and writes it with TMA tile stores (optionally also the row's
 // log-sum-exp).
+// Explicit masks: MODE_MASK reads the additive values; MODE_MASKB reads the bits of a binary
+// mask packed by mask_pack_kernel and visits only the key tiles that some row of the query
+// tile keeps (the key-tile bitmap walked like the sparse union).
 // Values computed before the warp-role split reach the roles through shared
 // memory or are recomputed: the producer warpgroup's setmaxnreg.dec may drop
 // registers above its new limit.
@@ -113,6 +116,14 @@ struct BlockWalk {
     rb &= rb - 1u;
     return w * 32 + t;
   }
+  // passes over the first n set bits; the bitmap must hold more than n
+  __device__ void skip(int n) {
+    while (n >= __popc(rb)) {
+      n -= __popc(rb);
+      rb = bm[++w];
+    }
+    for (; n > 0; --n) rb &= rb - 1u;
+  }
 };
 
 __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&x)[128]) {
@@ -145,6 +156,10 @@ __device__ __forceinline__ void store_out32(const AttnArgs& a, long long off, co
 template <int MODE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnArgs a) {
+  // a packed explicit mask is launched as bits, then as values: the launch that does not match
+  // the packing pass's verdict returns before it touches anything (the whole CTA alike)
+  if (MODE == MODE_MASKB && __ldg(a.mask_nonbinary) != 0) return;
+  if (MODE == MODE_MASK && a.mask_nonbinary != nullptr && __ldg(a.mask_nonbinary) == 0) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -244,6 +259,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int base = cnt;
     if (lane == 0) *n_ex_slot = base;
   }
+  if (MODE == MODE_MASKB && warp == 8) {
+    // A binary mask visits only the key tiles that some row of this query tile keeps (the
+    // others add exactly nothing); -1 in the slot means every key tile.
+    int cnt = -1;
+    if (a.mask_tiles != nullptr) {
+      uint32_t* bm = reinterpret_cast<uint32_t*>(smem + SM_BM);
+      const uint32_t* src = a.mask_tiles + (long long)qt * a.mask_tile_words;
+      cnt = 0;
+      for (int w = lane; w < a.mask_tile_words; w += 32) {
+        const uint32_t v = __ldg(src + w);
+        bm[w] = v;
+        cnt += __popc(v);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    }
+    if (lane == 0) *n_ex_slot = cnt;
+  }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -258,6 +291,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     n_tiles = ob + 1;
   } else if (MODE == MODE_MASK) {
     n_tiles = (a.T + kTile - 1) / kTile;
+  } else if (MODE == MODE_MASKB) {
+    n_tiles = *n_ex_slot >= 0 ? *n_ex_slot : (a.T + kTile - 1) / kTile;
   } else {
     n_pool = (ob + kTile - 1) / kTile;
     n_tiles = n_pool + *n_ex_slot;
@@ -290,8 +325,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int last_k[NSK], last_v[NSV];
       for (int st = 0; st < NSK; ++st) last_k[st] = -1;
       for (int st = 0; st < NSV; ++st) last_v[st] = -1;
+      // key tiles come from the kept-block bitmap (sparse, binary masks) or in order
+      const bool walked = MODE == MODE_SPARSE || (MODE == MODE_MASKB && *n_ex_slot >= 0);
       BlockWalk walk;
-      if (MODE == MODE_SPARSE) walk.init(kept_bm);
+      if (walked) walk.init(kept_bm);
+      if (walked && n_tiles > 0) walk.skip(j0);
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NSK, use = j / NSK;
         const int sv = j % NSV, usev = j / NSV;
@@ -303,7 +341,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           c1 = j * kTile;
           c2 = g;
         } else {
-          const int kt = (MODE == MODE_SPARSE) ? walk.next() : j0 + j;
+          const int kt = walked ? walk.next() : j0 + j;
           if (kt < a.n_hist_tiles) {
             mk = &maps.kh;
             mv = &maps.vh;
@@ -466,17 +504,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bits_row = a.row_bits + ((long long)(b * a.Hq + h) * a.C + row) * a.words;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    // binary explicit mask read as bits (one 16-byte word group per row and tile)
+    // MODE_MASKB: one 16-byte word group of mask bits per row and key tile, loaded before the
+    // step's score wait (padding rows read none and mask nothing).  Loading a step ahead
+    // instead holds four more registers across the loop and spills: slower.
     const uint4* mbits = nullptr;
-    if (MODE == MODE_MASK && a.mask_bits != nullptr && valid && __ldg(a.mask_binary) != 0)
+    if (MODE == MODE_MASKB && valid)
       mbits = reinterpret_cast<const uint4*>(a.mask_bits + (long long)row * a.mask_words);
-    uint4 nbits = make_uint4(0u, 0u, 0u, 0u);  // the next tile's mask bits, loaded a tile ahead
-    if (MODE == MODE_MASK && mbits != nullptr) nbits = __ldg(mbits + j0);
+    const bool mwalk = MODE == MODE_MASKB && *n_ex_slot >= 0;
     BlockWalk walk;
-    if (MODE == MODE_SPARSE) walk.init(kept_bm);
+    if (MODE == MODE_SPARSE || mwalk) walk.init(kept_bm);
+    if (mwalk && n_tiles > 0) walk.skip(j0);
     for (int j = 0; j < n_tiles; ++j) {
-      const uint4 bw = nbits;
-      if (MODE == MODE_MASK && mbits != nullptr && j + 1 < n_tiles) nbits = __ldg(mbits + (j0 + j + 1));
+      uint4 bw = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+      if (MODE == MODE_MASKB) {
+        const int kt = mwalk ? walk.next() : j0 + j;
+        if (mbits != nullptr) bw = __ldg(mbits + kt);
+      }
       ok = wait_all(BAR(B_SF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
                     (R_SOFT << 8) | (B_SF + sl));
       if (!ok) break;
@@ -491,7 +534,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c > r) x[c] = -INFINITY;
         }
-      } else if (MODE == MODE_MASK && mbits != nullptr) {
+      } else if (MODE == MODE_MASKB) {
         // bit set = kept (value 0); dropped keys (and keys past T, whose bits are 0) are -inf
         const uint32_t wq[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
@@ -708,7 +751,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_ld32(t_o + c0, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) wp[(long long)(c0 + i) * kTile + r] = __uint_as_float(o[i]);
+          for (int i = 0; i < 32; ++i)  // a part with no key tile holds O = 0 (TMEM never written)
+            wp[(long long)(c0 + i) * kTile + r] = n_tiles > 0 ? __uint_as_float(o[i]) : 0.f;
         }
         wp[(long long)a.d * kTile + r] = m;
         wp[(long long)(a.d + 1) * kTile + r] = l;
@@ -765,14 +809,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // One CTA per mask row (rows past 65535 loop): warp-wide loads of 32 consecutive values
 // become one word through a ballot; the row's kept count decides whether a fully dropped row
-// (a plain softmax over the raw scores with values, NaN with bits) forces the value path.
+// (a plain softmax over the raw scores with values, NaN with bits) forces the value path; the
+// key tiles the row keeps are ORed into its query tile's tile bitmap (when tiles != null).
 __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__ mask, int f16, int C,
                                                         int T, long long ld, uint32_t* __restrict__ bits,
-                                                        int words, int* binary) {
+                                                        int words, int* nonbinary, uint32_t* tiles,
+                                                        int tile_words) {
   __shared__ int kept_any;
+  __shared__ uint32_t row_tiles[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int row = blockIdx.y; row < C; row += gridDim.y) {
     if (threadIdx.x == 0) kept_any = 0;
+    for (int t = threadIdx.x; t < 64; t += blockDim.x) row_tiles[t] = 0u;
     __syncthreads();
     bool nonbin = false, any = false;
     for (int w = warp; w < words; w += blockDim.x / 32) {
@@ -787,12 +835,18 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__
       }
       const uint32_t word = __ballot_sync(0xffffffffu, keep);
       any |= word != 0u;
-      if (lane == 0) bits[(long long)row * words + w] = word;
+      if (lane == 0) {
+        bits[(long long)row * words + w] = word;
+        if (tiles != nullptr && word != 0u) atomicOr(&row_tiles[(w >> 2) >> 5], 1u << ((w >> 2) & 31));
+      }
     }
     if (__any_sync(0xffffffffu, any) && lane == 0) kept_any = 1;
-    if (__any_sync(0xffffffffu, nonbin) && lane == 0) atomicExch(binary, 0);
+    if (__any_sync(0xffffffffu, nonbin) && lane == 0) atomicExch(nonbinary, 1);
     __syncthreads();
-    if (threadIdx.x == 0 && !kept_any) atomicExch(binary, 0);
+    if (threadIdx.x == 0 && !kept_any) atomicExch(nonbinary, 1);
+    if (tiles != nullptr)
+      for (int t = threadIdx.x; t < tile_words; t += blockDim.x)
+        if (row_tiles[t] != 0u) atomicOr(&tiles[(long long)(row / kTile) * tile_words + t], row_tiles[t]);
     __syncthreads();
   }
 }
@@ -837,14 +891,15 @@ cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaS
   switch (mode) {
     case MODE_CAUSAL: return launch_mode<MODE_CAUSAL>(maps, a, st);
     case MODE_MASK: return launch_mode<MODE_MASK>(maps, a, st);
+    case MODE_MASKB: return launch_mode<MODE_MASKB>(maps, a, st);
     default: return launch_mode<MODE_SPARSE>(maps, a, st);
   }
 }
 
 cudaError_t launch_mask_pack(const void* mask, int f16, int C, int T, long long ld, uint32_t* bits,
-                             int words, int* binary, cudaStream_t st) {
+                             int words, int* nonbinary, uint32_t* tiles, int tile_words, cudaStream_t st) {
   const dim3 grid(1, C < 65535 ? C : 65535);
-  mask_pack_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, binary);
+  mask_pack_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, nonbinary, tiles, tile_words);
   ++t_launches;
   return cudaGetLastError();
 }

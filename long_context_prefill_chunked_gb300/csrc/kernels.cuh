@@ -10,7 +10,10 @@ constexpr int kTile = 128;        // query rows and keys per tile (= key block o
 constexpr int kMaxSplit = 8;      // parts of one split dense unit (tail split)
 constexpr int kAttnThreads = 384; // 8 softmax warps (2 slots x 4), TMA warp, MMA warp, 2 V converters
 
-enum AttnMode : int { MODE_CAUSAL = 0, MODE_MASK = 1, MODE_SPARSE = 2 };
+// MODE_MASKB: an explicit mask read as the packing pass's bits.  A packed mask is launched
+// twice, MODE_MASKB then MODE_MASK; each launch returns at once unless the pass's verdict on
+// the mask (binary or not) is its own, so each keeps its own register allocation.
+enum AttnMode : int { MODE_CAUSAL = 0, MODE_MASK = 1, MODE_SPARSE = 2, MODE_MASKB = 3 };
 
 struct AttnArgs {
   int B, Hq, Hkv, G, d, C, s, T;
@@ -27,10 +30,14 @@ struct AttnArgs {
   int mask_vec;         // rows 16-byte aligned: vector loads allowed
   long long mask_ld;    // elements between mask rows
   // the same mask packed to bits when every value is 0 or <= -10000 (bit set = kept);
-  // used only while *mask_binary != 0 (the packing pass clears it otherwise)
+  // used only while *mask_nonbinary == 0 (the packing pass sets it otherwise)
   const uint32_t* mask_bits;  // [C][mask_words], rows padded to a multiple of 4 words
   int mask_words;
-  const int* mask_binary;
+  const int* mask_nonbinary;
+  // per 128-row query tile, a bit per 128-key tile that some row of the tile keeps (binary
+  // masks only; null = visit every key tile)
+  const uint32_t* mask_tiles;  // [n_qt][mask_tile_words]
+  int mask_tile_words;
   // output
   void* out;
   float* lse;           // [B, Hq, C] log of each row's softmax denominator, or null
@@ -63,9 +70,10 @@ struct AttnMaps {
 
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaStream_t st);
 // Packs an additive mask [C, T] (row stride ld) into bits [C][words] (kept iff the value is 0)
-// and clears *binary when a value is neither 0 nor <= -10000 or a row keeps no key.
+// and sets *nonbinary when a value is neither 0 nor <= -10000 or a row keeps no key; with
+// tiles (zeroed, [ceil(C / 128)][tile_words]) it also ORs in the key tiles each query tile keeps.
 cudaError_t launch_mask_pack(const void* mask, int f16, int C, int T, long long ld, uint32_t* bits,
-                             int words, int* binary, cudaStream_t st);
+                             int words, int* nonbinary, uint32_t* tiles, int tile_words, cudaStream_t st);
 
 // bit copy of the chunk's K (or V) into the cache layout
 cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, int d,

@@ -265,8 +265,14 @@ pf_status pf_stream_status(void* stream) {
 
 long long mask_words_of(long long T) { return (T + kTile - 1) / kTile * 4; }
 
+long long mask_tile_words_of(long long T) { return ((T + kTile - 1) / kTile + 31) / 32; }
+
+long long mask_tiles_bytes(int C, long long T) {
+  return (((long long)C + kTile - 1) / kTile * mask_tile_words_of(T) * 4 + 255) / 256 * 256;
+}
+
 long long dense_masked_workspace_bytes(int d, int sms, int C, long long T) {
-  return dense_workspace_bytes(d, sms) + 256 + (long long)C * mask_words_of(T) * 4;
+  return dense_workspace_bytes(d, sms) + 256 + mask_tiles_bytes(C, T) + (long long)C * mask_words_of(T) * 4;
 }
 
 pf_status pf_dense_workspace_bytes_masked(const pf_shape* sh, int32_t start_pos, int64_t* bytes) {
@@ -371,24 +377,36 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
   plan_split(a, mode, workspace);
   if (mode == MODE_MASK && workspace != nullptr &&
       workspace_bytes >= dense_masked_workspace_bytes(d, sm_count(), C, (long long)s + C)) {
-    // binary masks (0 / <= -10000) are read as bits; the packing pass clears the flag and the
-    // kernels keep the value path when the mask is not binary
+    // binary masks (0 / <= -10000) are read as bits; the packing pass sets the flag and the
+    // kernels keep the value path when the mask is not binary.  Layout: the flag (256 bytes),
+    // the query tiles' key-tile bitmaps, the bits; one memset clears the first two.
     char* base = static_cast<char*>(workspace) + dense_workspace_bytes(d, sm_count());
+    const long long T = (long long)s + C;
+    const int words = (int)mask_words_of(T);
+    const int tile_words = (int)mask_tile_words_of(T);
+    const long long tile_bytes = mask_tiles_bytes(C, T);
     int* flag = reinterpret_cast<int*>(base);
-    uint32_t* bits = reinterpret_cast<uint32_t*>(base + 256);
-    const int words = (int)mask_words_of((long long)s + C);
-    if ((e = cudaMemsetAsync(flag, 1, sizeof(int), st)) != cudaSuccess) return cuda_fail(e, "mask flag");
-    if ((e = launch_mask_pack(mask, a.mask_f16, C, s + C, a.mask_ld, bits, words, flag, st)) != cudaSuccess)
+    uint32_t* bits = reinterpret_cast<uint32_t*>(base + 256 + tile_bytes);
+    // key-tile skipping needs the tile bitmap of a query tile in the kernel's 64-word bitmap
+    uint32_t* tiles = tile_words <= 64 ? reinterpret_cast<uint32_t*>(base + 256) : nullptr;
+    if ((e = cudaMemsetAsync(flag, 0, (size_t)(256 + (tiles != nullptr ? tile_bytes : 0)), st)) != cudaSuccess)
+      return cuda_fail(e, "mask flag and tile bitmap");
+    if ((e = launch_mask_pack(mask, a.mask_f16, C, (int)T, a.mask_ld, bits, words, flag, tiles, tile_words,
+                              st)) != cudaSuccess)
       return cuda_fail(e, "mask packing launch");
     a.mask_bits = bits;
     a.mask_words = words;
-    a.mask_binary = flag;
+    a.mask_nonbinary = flag;
+    a.mask_tiles = tiles;
+    a.mask_tile_words = tile_words;
   }
   if (a.split_k > 1) {
     const int n_split = a.n_qt * a.n_hp * a.B - a.n_whole;
     if ((e = cudaMemsetAsync(a.ws_cnt, 0, sizeof(int) * n_split, st)) != cudaSuccess)
       return cuda_fail(e, "workspace counters");
   }
+  if (a.mask_nonbinary != nullptr && (e = launch_attn(maps, a, MODE_MASKB, st)) != cudaSuccess)
+    return cuda_fail(e, "attention launch (mask bits)");
   e = launch_attn(maps, a, mode, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (out_k != nullptr) {

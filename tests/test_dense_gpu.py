@@ -153,6 +153,9 @@ def test_launch_counter_counts_kernels():
     pfx.launch_count(reset=True)
     run_chunk(w, 0, None, out_kv=True)
     assert pfx.launch_count() == 3      # attention + two cache-layout copies
+    pfx.launch_count(reset=True)
+    run_chunk(w, 0, pi.causal_mask(w.chunk, 0))
+    assert pfx.launch_count() == 3      # mask packing, the bits launch, the values launch
 
 
 def test_value_outside_fp16_range_is_reported():
@@ -204,6 +207,55 @@ def test_tail_split_matches_oracle_and_unsplit(case):
         assert_close(whole, ref, "whole " + case)
     mx, _ = errors(split, whole.double().cpu().numpy())
     assert mx <= 2e-3
+
+
+def _tile_sparse_mask(seed, C, T, keep_tiles):
+    """Binary mask where query tile i keeps keep_tiles[i] random key tiles (each key of those
+    kept with probability 0.6) and drops every other key; every row keeps at least one key."""
+    g = np.random.default_rng(seed)
+    nkt = -(-T // 128)
+    mask = np.full((C, T), -30000.0, dtype=np.float32)
+    for qt, n in enumerate(keep_tiles):
+        r0, r1 = qt * 128, min(C, qt * 128 + 128)
+        tiles = g.choice(nkt, n, replace=False)
+        for t in tiles:
+            blk = mask[r0:r1, t * 128:min(T, t * 128 + 128)]
+            blk[g.random(blk.shape) < 0.6] = 0.0
+        mask[r0:r1, tiles[0] * 128] = 0.0
+    return mask
+
+
+@pytest.mark.parametrize("workspace", [True, None])
+def test_binary_mask_skips_dropped_key_tiles(workspace):
+    """A binary mask that drops whole 128-key tiles for a query tile: with the workspace the
+    packed path visits only the kept tiles (query tiles keeping 1 or 2 of 24 tiles leave tail
+    split parts with no tile at all); without it every tile is read through the mask values.
+    Both against the oracle."""
+    C, s = 1000, 2048
+    w = pi.normal_workload("tile-skip", 81, 1, 8, 2, 128, s + C, C, "bf16")
+    mask = _tile_sparse_mask(82, C, s + C, [1, 2, 3, 5, 24, 8, 1, 13])
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(s))
+    lse = torch.empty((1, 8, C), dtype=torch.float32, device="cuda")
+    out = pfx.attn_dense(q, kh, vh, kc, vc, s, mask=torch.from_numpy(mask).cuda(), lse=lse,
+                         workspace=workspace)
+    pfx.stream_status()
+    ref, rlse = oracle.dense(*(w.f64(x) for x in w.chunk_views(s)), s, mask=mask.astype(np.float64),
+                             with_lse=True)
+    assert_close(out, ref, "tile-sparse mask, workspace %s" % workspace)
+    got = lse.cpu().double().numpy().transpose(0, 2, 1)
+    assert np.max(np.abs(got - rlse)) <= LSE_TOL
+
+
+def test_binary_mask_past_the_tile_bitmap_visits_every_tile():
+    """start_pos + C = 262272 keys is 2050 key tiles, more than a query tile's 2048-bit bitmap:
+    the packed bits are still used but every key tile is visited.  Sampled rows."""
+    C, s = 200, 262144
+    w = pi.normal_workload("tile-bitmap-cap", 83, 1, 2, 1, 128, s + C, C, "bf16")
+    mask = _tile_sparse_mask(84, C, s + C, [40, 3])
+    rows = np.array([0, 1, 63, 127, 128, 150, 199])
+    out, _, _ = run_chunk(w, s, mask)
+    ref = ref_chunk(w, s, mask, rows=rows)
+    assert_close(out[:, rows], ref, "2050 key tiles")
 
 
 def test_tail_split_workspace_too_small_is_refused():
