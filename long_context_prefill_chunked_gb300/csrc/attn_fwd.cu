@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const bool walked = MODE == MODE_SPARSE || (MODE == MODE_MASKB && *n_ex_slot >= 0);
       BlockWalk walk;
       if (walked) walk.init(kept_bm);
-      if (walked && n_tiles > 0) walk.skip(j0);
+      if (MODE == MODE_MASKB && walked && n_tiles > 0) walk.skip(j0);  // sparse units never split
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NSK, use = j / NSK;
         const int sv = j % NSV, usev = j / NSV;
