@@ -5,8 +5,9 @@ and reference legs may import this package.  It shares no code with the CUDA
 library and never calls it.
 """
 from .attention import (MASK_DROP, KeepRules, Selection, block_counts, block_select,
-                        causal_additive, chunk_kv_cache_layout, dense, pool_blocks, skip_share,
-                        sparse, tile_union)
+                        causal_additive, chunk_kv_cache_layout, dense, dense_indexed,
+                        indexed_visible_keys, pool_blocks, skip_share, sparse, tile_union)
 
 __all__ = ["MASK_DROP", "KeepRules", "Selection", "block_counts", "block_select", "causal_additive",
-           "chunk_kv_cache_layout", "dense", "pool_blocks", "skip_share", "sparse", "tile_union"]
+           "chunk_kv_cache_layout", "dense", "dense_indexed", "indexed_visible_keys", "pool_blocks",
+           "skip_share", "sparse", "tile_union"]

@@ -20,7 +20,9 @@ Sources (page title, section):
     of queries attends to a token-major K/V history plus its own keys, under
     an additive mask; the chunk's K/V are returned in cache layout) and
     "Folding a sparse indexer's selection into the mask" (dropped keys carry
-    -30000, which exp() turns into an exact zero).
+    -30000, which exp() turns into an exact zero; the indexer's keep lists name
+    compressed blocks of keys, and the keys after the last complete block stay
+    visible).
   * "The Four Principles for Optimizing Transformers on the ANE", section
     "Masking in this layout" (masks are additive floats applied before the
     softmax).
@@ -117,6 +119,70 @@ def dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, scale=None,
                 den = w.sum(axis=1, keepdims=True)
                 out[b, r0:r0 + len(rr), hi, :] = (w @ vg) / den
                 lse[b, r0:r0 + len(rr), hi] = m[:, 0] + np.log(den[:, 0])
+    return (out, lse) if with_lse else out
+
+
+def indexed_visible_keys(p: int, kept, ratio: int) -> np.ndarray:
+    """The keys an indexer's compacted selection leaves visible to the query at position p.
+
+    "ANE Prefill Research", section "Folding a sparse indexer's selection into the
+    mask": the indexer keeps compressed blocks (keepIndices / keepCounts); block c
+    covers keys ratio*c .. ratio*c + ratio - 1, and the keys after the last complete
+    block, ratio*floor((p+1)/ratio) .. p, stay visible uncompressed (the pages' budget
+    keptBlocks x compressRatio + (compressRatio - 1) counts them).  A kept block must
+    be complete (c < floor((p+1)/ratio)); anything else is an error.  Returns the
+    sorted distinct key indices.
+    """
+    if ratio < 1:
+        raise ValueError("ratio %d < 1" % ratio)
+    n_complete = (p + 1) // ratio
+    kept = np.asarray(kept, dtype=np.int64).reshape(-1)
+    if kept.size and (kept.min() < 0 or kept.max() >= n_complete):
+        raise ValueError("kept block outside the %d complete blocks of position %d" % (n_complete, p))
+    keys = (kept[:, None] * ratio + np.arange(ratio)[None, :]).reshape(-1)
+    tail = np.arange(n_complete * ratio, p + 1)
+    visible = np.unique(np.concatenate([keys, tail]))
+    if visible.size == 0:
+        raise ValueError("position %d sees no key" % p)
+    return visible
+
+
+def dense_indexed(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, kept, ratio, scale=None,
+                  rows=None, heads=None, with_lse=False):
+    """Attention of a chunk over the keys an indexer kept, gathered per row.
+
+    Row i (position p = start_pos + i) attends only to indexed_visible_keys(p,
+    kept[i], ratio) of [history ; chunk]: o_i = sum_j exp(l_j - m) v_j / sum_j
+    exp(l_j - m) over those keys j, l_j = (q_i . k_j) * scale.  The keys are
+    gathered, no mask is formed; the pages state that folding the same selection
+    into an additive mask as -30000 gives the same result, since exp() of such a
+    logit is zero.  kept: a list of C index arrays.  Shapes and return as dense().
+    """
+    B, C, Hq, d = q.shape
+    Hkv = k_chunk.shape[2]
+    G = Hq // Hkv
+    s = int(start_pos)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if len(kept) != C:
+        raise ValueError("kept holds %d rows, expected %d" % (len(kept), C))
+    k = np.concatenate([k_hist, k_chunk], axis=1)
+    v = np.concatenate([v_hist, v_chunk], axis=1)
+    rows = _rows_arg(rows, C)
+    heads = _heads_arg(heads, Hq)
+    out = np.empty((B, len(rows), len(heads), d))
+    lse = np.empty((B, len(rows), len(heads)))
+    for ri, i in enumerate(rows):
+        js = indexed_visible_keys(s + int(i), kept[int(i)], ratio)
+        for b in range(B):
+            for hi, h in enumerate(heads):
+                g = h // G
+                logits = (k[b, js, g, :] @ q[b, i, h, :]) * scale
+                m = logits.max()
+                w = np.exp(logits - m)
+                den = w.sum()
+                out[b, ri, hi, :] = (w @ v[b, js, g, :]) / den
+                lse[b, ri, hi] = m + math.log(den)
     return (out, lse) if with_lse else out
 
 

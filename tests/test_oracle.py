@@ -189,6 +189,106 @@ def test_folded_mask_visible_budget():
 
 
 # --------------------------------------------------------------------------
+# index-driven attention (the indexer's keep lists, gathered)
+# --------------------------------------------------------------------------
+def _visible_by_predicate(p, kept, ratio):
+    """Key j is visible iff its compressed block is kept and complete, or j lies after the
+    last complete block and not after p (a membership test, not the oracle's construction)."""
+    n_complete = (p + 1) // ratio
+    kept = set(int(c) for c in kept)
+    return [j for j in range(p + 1)
+            if (j // ratio in kept and j // ratio < n_complete) or n_complete * ratio <= j <= p]
+
+
+@pytest.mark.parametrize("ratio", [3, 4])
+def test_indexed_matches_brute_force_over_the_visible_keys(ratio):
+    q, kh, vh, kc, vc = rand_case(11, B=1, Hq=4, Hkv=2, C=6, s=12, d=8)
+    B, C, Hq, d = q.shape
+    s = kh.shape[1]
+    g = np.random.default_rng(12)
+    kept = [g.choice((s + i + 1) // ratio, size=min(2, (s + i + 1) // ratio), replace=False)
+            for i in range(C)]
+    out = oracle.dense_indexed(q, kh, vh, kc, vc, s, kept, ratio)
+    k = np.concatenate([kh, kc], axis=1)
+    v = np.concatenate([vh, vc], axis=1)
+    for i in range(C):
+        js = _visible_by_predicate(s + i, kept[i], ratio)
+        for h in range(Hq):
+            gk = h // (Hq // kh.shape[2])
+            ref = brute_dense_row(q[0, i, h], [k[0, j, gk] for j in js], [v[0, j, gk] for j in js],
+                                  [0.0] * len(js), 1.0 / math.sqrt(d))
+            assert np.max(np.abs(out[0, i, h] - ref)) < 1e-12
+
+
+def test_indexed_equals_the_folded_mask():
+    """The pages fold the same selection into an additive mask at -30000: same result."""
+    s, C, ratio, nk = 256, 64, 4, 16
+    q, kh, vh, kc, vc = rand_case(13, B=1, Hq=4, Hkv=2, C=C, s=s, d=16)
+    mask, kept = pi.indexer_fold_mask(14, C, s, kept_blocks=nk, ratio=ratio)
+    a = oracle.dense(q, kh, vh, kc, vc, s, mask=mask.astype(np.float64))
+    b = oracle.dense_indexed(q, kh, vh, kc, vc, s, kept, ratio)
+    assert np.max(np.abs(a - b)) < 1e-12
+
+
+def test_indexed_all_complete_blocks_is_causal():
+    s, C, ratio = 20, 9, 4
+    q, kh, vh, kc, vc = rand_case(15, B=2, Hq=2, Hkv=1, C=C, s=s, d=8)
+    kept = [np.arange((s + i + 1) // ratio) for i in range(C)]
+    a = oracle.dense(q, kh, vh, kc, vc, s)
+    b = oracle.dense_indexed(q, kh, vh, kc, vc, s, kept, ratio)
+    assert np.max(np.abs(a - b)) < 1e-12
+
+
+@pytest.mark.parametrize("ratio", [3, 4, 5])
+def test_indexed_visible_count(ratio):
+    """keptBlocks x ratio + ((p + 1) mod ratio) keys; duplicates and order change nothing."""
+    g = np.random.default_rng(16)
+    for p in range(40, 60):
+        nc = (p + 1) // ratio
+        kept = g.choice(nc, size=5, replace=False)
+        vis = oracle.indexed_visible_keys(p, kept, ratio)
+        assert len(vis) == 5 * ratio + (p + 1) % ratio
+        assert vis.max() <= p
+        dup = np.concatenate([kept[::-1], kept[:2]])
+        assert np.array_equal(oracle.indexed_visible_keys(p, dup, ratio), vis)
+
+
+def test_indexed_rejects_a_bad_selection():
+    with pytest.raises(ValueError):
+        oracle.indexed_visible_keys(10, [2], 4)       # block 2 holds keys 8..11: not complete at 10
+    with pytest.raises(ValueError):
+        oracle.indexed_visible_keys(10, [-1], 4)
+    with pytest.raises(ValueError):
+        oracle.indexed_visible_keys(11, [], 4)        # 12 keys in 3 complete blocks, none kept
+    assert list(oracle.indexed_visible_keys(10, [], 4)) == [8, 9, 10]
+
+
+def test_indexed_single_key_returns_its_value_and_lse():
+    """A row whose only visible key is its own (p + 1 = 1 mod ratio, nothing kept): out = v_p,
+    lse = (q . k_p) * scale."""
+    s, C, ratio = 8, 1, 4                              # p = 8: tail = key 8 alone
+    q, kh, vh, kc, vc = rand_case(17, B=1, Hq=2, Hkv=2, C=C, s=s, d=8)
+    out, lse = oracle.dense_indexed(q, kh, vh, kc, vc, s, [np.array([], dtype=np.int64)], ratio,
+                                    with_lse=True)
+    assert np.array_equal(out[0, 0], vc[0, 0])
+    for h in range(2):
+        assert abs(lse[0, 0, h] - float(q[0, 0, h] @ kc[0, 0, h]) / math.sqrt(8)) < 1e-12
+
+
+def test_indexed_lse_identical_keys_closed_form():
+    """All keys equal: lse = log(visible count) + (q . k) * scale."""
+    s, C, ratio = 16, 4, 4
+    q, kh, vh, kc, vc = rand_case(18, B=1, Hq=1, Hkv=1, C=C, s=s, d=4)
+    kh[:] = 0.25
+    kc[:] = 0.25
+    kept = [np.array([0, 2]), np.array([1]), np.array([], dtype=np.int64), np.array([0, 1, 3])]
+    _, lse = oracle.dense_indexed(q, kh, vh, kc, vc, s, kept, ratio, with_lse=True)
+    for i in range(C):
+        n = len(kept[i]) * ratio + (s + i + 1) % ratio
+        assert abs(lse[0, i, 0] - (math.log(n) + q[0, i, 0].sum() * 0.25 / 2.0)) < 1e-12
+
+
+# --------------------------------------------------------------------------
 # block-sparse path
 # --------------------------------------------------------------------------
 def toy36(e_scale=1.0):
