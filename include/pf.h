@@ -134,6 +134,33 @@ pf_status pf_dense_workspace_bytes(const pf_shape* shape, int64_t* bytes);
  * values. */
 pf_status pf_dense_workspace_bytes_masked(const pf_shape* shape, int32_t start_pos, int64_t* bytes);
 
+/* Index-driven attention over an indexer's compacted selection ("ANE Prefill Research",
+ * section "Folding a sparse indexer's selection into the mask": keepIndices / keepCounts).
+ * Row i (position p = start_pos + i) attends only to
+ *   - the keys of its kept compressed blocks: block c covers keys ratio*c .. ratio*c + ratio - 1
+ *     of [history ; chunk], and must be complete at the row, 0 <= c < floor((p + 1) / ratio);
+ *   - the keys after the last complete block, ratio*floor((p + 1) / ratio) .. p.
+ * The result equals pf_attn_dense with that selection folded into a 0 / -30000 mask, but no
+ * [C, start_pos + C] mask is written or read: the lists are packed to bits on the device and
+ * only the 128-key tiles that some row of a query tile sees are visited.
+ * keep_idx [C][keep_stride] int32 (device, 4-byte aligned): row i's entries are its first
+ * keep_cnt[i]; their order does not matter and a repeated entry counts once.
+ * keep_cnt [C] int32 (device).  ratio in [1, 128] (PF_EINVAL otherwise).
+ * start_pos + C <= 1048576 (PF_EUNSUPPORTED otherwise).
+ * workspace is required: workspace_bytes >= pf_indexed_workspace_bytes (PF_EINVAL otherwise).
+ * An entry outside the row's complete blocks, a count outside [0, keep_stride] or a row that
+ * sees no key cannot be checked on the host: the entry is skipped, the output is invalid, and
+ * the next pf_stream_status returns PF_EINVAL.
+ * Every other argument as pf_attn_dense (shape->mask_dtype and mask_ld are not used). */
+pf_status pf_attn_indexed(const pf_shape* shape, const void* q, const void* k_hist,
+                          const void* v_hist, const void* k_chunk, const void* v_chunk,
+                          const int32_t* keep_idx, const int32_t* keep_cnt, int32_t keep_stride,
+                          int32_t ratio, int32_t start_pos, void* out, float* lse, void* out_k,
+                          void* out_v, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes for pf_attn_indexed (the same as pf_dense_workspace_bytes_masked). */
+pf_status pf_indexed_workspace_bytes(const pf_shape* shape, int32_t start_pos, int64_t* bytes);
+
 /* Block selection produced by pf_block_index and consumed by pf_attn_sparse.
  * nblk = ceil((start_pos + C) / block); nqt = ceil(C / 128); W = ceil(nblk / 32). */
 typedef struct {
@@ -233,9 +260,10 @@ pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void
                                 const pf_sel* sel, void* out, float* lse, void* stream);
 
 /* Synchronise `stream`, then report (and clear) a device-side error: PF_ETIMEOUT
- * if a bounded wait in a kernel gave up since the last check; PF_ERANGE if a
- * bf16 v held a value the fp16 P*V product cannot represent (|v| > 65504, inf or
- * nan: the output is then invalid); PF_ECUDA on a CUDA error; else PF_OK. */
+ * if a bounded wait in a kernel gave up since the last check; PF_EINVAL if a
+ * pf_attn_indexed selection was invalid; PF_ERANGE if a bf16 v held a value the
+ * fp16 P*V product cannot represent (|v| > 65504, inf or nan); the output of the
+ * call concerned is then invalid.  PF_ECUDA on a CUDA error; else PF_OK. */
 pf_status pf_stream_status(void* stream);
 
 /* Bounded-wait limit in SM clock cycles (default 4e8, about 0.2 s). */

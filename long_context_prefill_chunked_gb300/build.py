@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libpf.so")
-SOURCES = ["pf_abi.cu", "attn_fwd.cu", "pool_index.cu", "index_tc.cu", "pf_static.cu"]
+SOURCES = ["pf_abi.cu", "attn_fwd.cu", "pool_index.cu", "index_tc.cu", "pf_static.cu", "indexed.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -1,0 +1,98 @@
+// Packs an indexer's keep lists into per-row key bits and per-query-tile key-tile bitmaps.
+//
+// Method: "ANE Prefill Research", section "Folding a sparse indexer's selection into the
+// mask": the indexer keeps compressed key blocks per query (keepIndices / keepCounts) and the
+// keys after the last complete block stay visible.  The pages fold that selection into an
+// additive mask of -30000; here it becomes the bit form of the same mask directly (no [C, T]
+// float mask is written or read), which the attention kernel's bits mode consumes, skipping
+// the 128-key tiles no row of a query tile sees.
+#include "indexed.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace pf {
+namespace {
+
+// sets key bits [k0, k1) of a shared-memory row
+__device__ __forceinline__ void set_key_range(uint32_t* rw, int k0, int k1) {
+  while (k0 < k1) {
+    const int b = k0 & 31;
+    const int n = min(k1 - k0, 32 - b);
+    const uint32_t m = (n == 32 ? 0xffffffffu : ((1u << n) - 1u)) << b;
+    atomicOr(&rw[k0 >> 5], m);
+    k0 += n;
+  }
+}
+
+// One CTA per row (rows past the grid loop): the row's bits are built in shared memory, then
+// written 16 bytes (one 128-key tile) per thread; a warp's 32 consecutive tiles become one
+// tile-bitmap word through a ballot.
+__global__ void __launch_bounds__(256) index_pack_kernel(const int32_t* __restrict__ keep_idx,
+                                                         const int32_t* __restrict__ keep_cnt,
+                                                         long long stride, int ratio, int C, int s,
+                                                         uint32_t* __restrict__ bits, int words,
+                                                         uint32_t* tiles, int tile_words,
+                                                         unsigned* status) {
+  extern __shared__ uint32_t rw[];
+  const int n_kt = words / 4;
+  for (int row = blockIdx.x; row < C; row += gridDim.x) {
+    const int p = s + row;
+    const int n_complete = (p + 1) / ratio;
+    for (int w = threadIdx.x; w < words; w += blockDim.x) rw[w] = 0u;
+    __syncthreads();
+    int cnt = __ldg(keep_cnt + row);
+    bool bad = cnt < 0 || cnt > stride;
+    cnt = cnt < 0 ? 0 : (cnt > stride ? (int)stride : cnt);
+    const int32_t* list = keep_idx + (long long)row * stride;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      const int c = __ldg(list + i);
+      if (c < 0 || c >= n_complete) {
+        bad = true;
+        continue;
+      }
+      set_key_range(rw, c * ratio, c * ratio + ratio);
+    }
+    if (threadIdx.x == 0) set_key_range(rw, n_complete * ratio, p + 1);
+    __syncthreads();
+    bool any = false;
+    uint4* out = reinterpret_cast<uint4*>(bits + (long long)row * words);
+    for (int t0 = 0; t0 < n_kt; t0 += blockDim.x) {
+      const int t = t0 + threadIdx.x;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (t < n_kt) {
+        v = make_uint4(rw[4 * t], rw[4 * t + 1], rw[4 * t + 2], rw[4 * t + 3]);
+        out[t] = v;
+      }
+      const bool seen = (v.x | v.y | v.z | v.w) != 0u;
+      any |= seen;
+      const uint32_t word = __ballot_sync(0xffffffffu, seen);
+      if (tiles != nullptr && (threadIdx.x & 31) == 0 && word != 0u)
+        atomicOr(&tiles[(long long)(row >> 7) * tile_words + (t >> 5)], word);
+    }
+    if (bad) record_error(status, ST_SELECTION, 0x500u);
+    // also the barrier before the next row clears the shared row
+    if (__syncthreads_or(any) == 0 && threadIdx.x == 0) record_error(status, ST_SELECTION, 0x501u);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_index_pack(const int32_t* keep_idx, const int32_t* keep_cnt, long long stride,
+                              int ratio, int C, int s, uint32_t* bits, int words, uint32_t* tiles,
+                              int tile_words, unsigned* status, cudaStream_t st) {
+  const size_t smem = (size_t)words * 4;
+  static size_t configured = 48 * 1024;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(index_pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  const int grid = C < 152 * 8 ? C : 152 * 8;
+  index_pack_kernel<<<grid, 256, smem, st>>>(keep_idx, keep_cnt, stride, ratio, C, s, bits, words, tiles,
+                                             tile_words, status);
+  ++t_launches;
+  return cudaGetLastError();
+}
+
+}  // namespace pf

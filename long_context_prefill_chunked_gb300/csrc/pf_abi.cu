@@ -7,6 +7,7 @@
 
 #include <string>
 
+#include "indexed.cuh"
 #include "kernels.cuh"
 #include "pf.h"
 #include "ptx.cuh"
@@ -208,6 +209,20 @@ long long dense_workspace_bytes(int d, int sms) {
   return kCountBytes + (long long)sms * 2 * kTile * (d + 2) * 4;
 }
 
+// The masked workspace: the dense one, then a 256-byte flag area, the query tiles' key-tile
+// bitmaps and the packed mask bits [C][mask_words] (4 words = 128 keys per tile).
+long long mask_words_of(long long T) { return (T + kTile - 1) / kTile * 4; }
+
+long long mask_tile_words_of(long long T) { return ((T + kTile - 1) / kTile + 31) / 32; }
+
+long long mask_tiles_bytes(int C, long long T) {
+  return (((long long)C + kTile - 1) / kTile * mask_tile_words_of(T) * 4 + 255) / 256 * 256;
+}
+
+long long dense_masked_workspace_bytes(int d, int sms, int C, long long T) {
+  return dense_workspace_bytes(d, sms) + 256 + mask_tiles_bytes(C, T) + (long long)C * mask_words_of(T) * 4;
+}
+
 // Tail split.  With U units and P SMs, the last wave holds W = U mod P units (all U when
 // U < P) on P SMs; each of those units (the lightest, since units run heaviest first) is
 // cut into k = P / W parts of consecutive key tiles so that the last wave fills the GPU.
@@ -231,73 +246,22 @@ void plan_split(AttnArgs& a, int mode, void* ws) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-const char* pf_last_error(void) { return t_err.c_str(); }
+// An indexer's keep lists (pf_attn_indexed).
+struct IndexSel {
+  const int32_t* keep_idx;
+  const int32_t* keep_cnt;
+  int32_t keep_stride;
+  int32_t ratio;
+};
 
-const char* pf_version(void) { return "libpf 0.1 sm_103a"; }
-
-void pf_set_wait_timeout(int64_t cycles) { g_timeout = cycles > 1000 ? cycles : 1000; }
-
-void pf_set_debug_withhold(int32_t on) { g_withhold = on ? 1 : 0; }
-
-int64_t pf_launch_count(int32_t reset) {
-  const long long n = t_launches;
-  if (reset) t_launches = 0;
-  return n;
-}
-
-pf_status pf_stream_status(void* stream) {
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  unsigned w[2] = {0, 0};
-  e = cudaMemcpyFromSymbol(w, g_status, sizeof(w));
-  if (e != cudaSuccess) return cuda_fail(e, "read status word");
-  if (w[0] == 0) return PF_OK;
-  const unsigned zero[2] = {0, 0};
-  cudaMemcpyToSymbol(g_status, zero, sizeof(zero));
-  if ((w[0] & ST_TIMEOUT) == 0u && (w[0] & ST_VRANGE) != 0u)
-    return fail(PF_ERANGE, "v holds a bf16 value outside the fp16 range of the P*V product "
-                           "(|v| > 65504, inf or nan)");
-  return fail(PF_ETIMEOUT, "a bounded device wait gave up (status 0x%x, role %u, barrier %u)", w[0],
-              w[1] >> 8, w[1] & 0xFFu);
-}
-
-long long mask_words_of(long long T) { return (T + kTile - 1) / kTile * 4; }
-
-long long mask_tile_words_of(long long T) { return ((T + kTile - 1) / kTile + 31) / 32; }
-
-long long mask_tiles_bytes(int C, long long T) {
-  return (((long long)C + kTile - 1) / kTile * mask_tile_words_of(T) * 4 + 255) / 256 * 256;
-}
-
-long long dense_masked_workspace_bytes(int d, int sms, int C, long long T) {
-  return dense_workspace_bytes(d, sms) + 256 + mask_tiles_bytes(C, T) + (long long)C * mask_words_of(T) * 4;
-}
-
-pf_status pf_dense_workspace_bytes_masked(const pf_shape* sh, int32_t start_pos, int64_t* bytes) {
-  if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
-  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
-  if (sh->C < 1 || start_pos < 0) return fail(PF_EINVAL, "C >= 1 and start_pos >= 0 required");
-  const int P = sm_count();
-  if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
-  *bytes = dense_masked_workspace_bytes(sh->d, P, sh->C, (long long)start_pos + sh->C);
-  return PF_OK;
-}
-
-pf_status pf_dense_workspace_bytes(const pf_shape* sh, int64_t* bytes) {
-  if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
-  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
-  const int P = sm_count();
-  if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
-  *bytes = dense_workspace_bytes(sh->d, P);
-  return PF_OK;
-}
-
-pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, const void* v_hist,
-                        const void* k_chunk, const void* v_chunk, const void* mask,
-                        int32_t start_pos, void* out, float* lse, void* out_k, void* out_v,
-                        void* workspace, int64_t workspace_bytes, void* stream) {
+// pf_attn_dense, and pf_attn_indexed when isel != null (then mask is null and the selection is
+// packed to bits in the workspace, which is required).
+pf_status dense_entry(const pf_shape* sh, const void* q, const void* k_hist, const void* v_hist,
+                      const void* k_chunk, const void* v_chunk, const void* mask, const IndexSel* isel,
+                      int32_t start_pos, void* out, float* lse, void* out_k, void* out_v,
+                      void* workspace, int64_t workspace_bytes, void* stream) {
   pf_status rc = check_common(sh, start_pos);
   if (rc != PF_OK) return rc;
   if (q == nullptr || k_chunk == nullptr || v_chunk == nullptr || out == nullptr)
@@ -307,12 +271,30 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
   if ((out_k == nullptr) != (out_v == nullptr)) return fail(PF_EINVAL, "give both out_k and out_v, or neither");
   if (mask != nullptr && sh->mask_dtype != PF_F32 && sh->mask_dtype != PF_F16)
     return fail(PF_EUNSUPPORTED, "mask dtype must be f32 or f16 (bf16 cannot hold -30000 exactly)");
+  if (isel != nullptr) {
+    if (isel->keep_cnt == nullptr || (isel->keep_idx == nullptr && isel->keep_stride > 0))
+      return fail(PF_EINVAL, "keep_cnt (and keep_idx when keep_stride > 0) must not be NULL");
+    if (isel->keep_stride < 0) return fail(PF_EINVAL, "keep_stride %d < 0", isel->keep_stride);
+    if (isel->ratio < 1 || isel->ratio > 128)
+      return fail(PF_EINVAL, "compression ratio %d outside [1, 128]", isel->ratio);
+    if ((reinterpret_cast<uintptr_t>(isel->keep_idx) & 3u) != 0u ||
+        (reinterpret_cast<uintptr_t>(isel->keep_cnt) & 3u) != 0u)
+      return fail(PF_EINVAL, "keep_idx and keep_cnt must be 4-byte aligned");
+    if ((long long)start_pos + sh->C > kIndexedMaxKeys)
+      return fail(PF_EUNSUPPORTED, "start_pos + C = %lld keys (index-driven attention supports %lld)",
+                  (long long)start_pos + sh->C, kIndexedMaxKeys);
+    if (workspace == nullptr) return fail(PF_EINVAL, "index-driven attention needs a workspace");
+  }
   if (workspace != nullptr) {
     const int P = sm_count();
     if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
     if (workspace_bytes < dense_workspace_bytes(sh->d, P))
       return fail(PF_EINVAL, "workspace of %lld bytes is smaller than pf_dense_workspace_bytes (%lld)",
                   (long long)workspace_bytes, dense_workspace_bytes(sh->d, P));
+    const long long need = dense_masked_workspace_bytes(sh->d, P, sh->C, (long long)start_pos + sh->C);
+    if (isel != nullptr && workspace_bytes < need)
+      return fail(PF_EINVAL, "workspace of %lld bytes is smaller than pf_indexed_workspace_bytes (%lld)",
+                  (long long)workspace_bytes, need);
   }
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0u)
     return fail(PF_EINVAL, "lse must be 4-byte aligned");
@@ -374,8 +356,9 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
   if (a.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (isel != nullptr) mode = MODE_MASKB;
   plan_split(a, mode, workspace);
-  if (mode == MODE_MASK && workspace != nullptr &&
+  if ((mode == MODE_MASK || mode == MODE_MASKB) && workspace != nullptr &&
       workspace_bytes >= dense_masked_workspace_bytes(d, sm_count(), C, (long long)s + C)) {
     // binary masks (0 / <= -10000) are read as bits; the packing pass sets the flag and the
     // kernels keep the value path when the mask is not binary.  Layout: the flag (256 bytes),
@@ -391,9 +374,15 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
     uint32_t* tiles = tile_words <= 64 ? reinterpret_cast<uint32_t*>(base + 256) : nullptr;
     if ((e = cudaMemsetAsync(flag, 0, (size_t)(256 + (tiles != nullptr ? tile_bytes : 0)), st)) != cudaSuccess)
       return cuda_fail(e, "mask flag and tile bitmap");
-    if ((e = launch_mask_pack(mask, a.mask_f16, C, (int)T, a.mask_ld, bits, words, flag, tiles, tile_words,
-                              st)) != cudaSuccess)
+    if (isel != nullptr) {
+      // the keep lists become bits directly; the flag stays 0 (bits valid by construction)
+      if ((e = launch_index_pack(isel->keep_idx, isel->keep_cnt, isel->keep_stride, isel->ratio, C, s,
+                                 bits, words, tiles, tile_words, a.status, st)) != cudaSuccess)
+        return cuda_fail(e, "keep-list packing launch");
+    } else if ((e = launch_mask_pack(mask, a.mask_f16, C, (int)T, a.mask_ld, bits, words, flag, tiles,
+                                     tile_words, st)) != cudaSuccess) {
       return cuda_fail(e, "mask packing launch");
+    }
     a.mask_bits = bits;
     a.mask_words = words;
     a.mask_nonbinary = flag;
@@ -405,7 +394,8 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
     if ((e = cudaMemsetAsync(a.ws_cnt, 0, sizeof(int) * n_split, st)) != cudaSuccess)
       return cuda_fail(e, "workspace counters");
   }
-  if (a.mask_nonbinary != nullptr && (e = launch_attn(maps, a, MODE_MASKB, st)) != cudaSuccess)
+  if (mode == MODE_MASK && a.mask_nonbinary != nullptr &&
+      (e = launch_attn(maps, a, MODE_MASKB, st)) != cudaSuccess)
     return cuda_fail(e, "attention launch (mask bits)");
   e = launch_attn(maps, a, mode, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -416,6 +406,84 @@ pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, c
       return cuda_fail(e, "out_v copy");
   }
   return PF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pf_last_error(void) { return t_err.c_str(); }
+
+const char* pf_version(void) { return "libpf 0.1 sm_103a"; }
+
+void pf_set_wait_timeout(int64_t cycles) { g_timeout = cycles > 1000 ? cycles : 1000; }
+
+void pf_set_debug_withhold(int32_t on) { g_withhold = on ? 1 : 0; }
+
+int64_t pf_launch_count(int32_t reset) {
+  const long long n = t_launches;
+  if (reset) t_launches = 0;
+  return n;
+}
+
+pf_status pf_stream_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned w[2] = {0, 0};
+  e = cudaMemcpyFromSymbol(w, g_status, sizeof(w));
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  if (w[0] == 0) return PF_OK;
+  const unsigned zero[2] = {0, 0};
+  cudaMemcpyToSymbol(g_status, zero, sizeof(zero));
+  if ((w[0] & ST_TIMEOUT) == 0u && (w[0] & ST_SELECTION) != 0u)
+    return fail(PF_EINVAL, "a keep list named a compressed block that is not complete at its row, a keep "
+                           "count was outside [0, keep_stride], or a row saw no key (output invalid)");
+  if ((w[0] & ST_TIMEOUT) == 0u && (w[0] & ST_VRANGE) != 0u)
+    return fail(PF_ERANGE, "v holds a bf16 value outside the fp16 range of the P*V product "
+                           "(|v| > 65504, inf or nan)");
+  return fail(PF_ETIMEOUT, "a bounded device wait gave up (status 0x%x, role %u, barrier %u)", w[0],
+              w[1] >> 8, w[1] & 0xFFu);
+}
+
+pf_status pf_dense_workspace_bytes_masked(const pf_shape* sh, int32_t start_pos, int64_t* bytes) {
+  if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
+  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  if (sh->C < 1 || start_pos < 0) return fail(PF_EINVAL, "C >= 1 and start_pos >= 0 required");
+  const int P = sm_count();
+  if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
+  *bytes = dense_masked_workspace_bytes(sh->d, P, sh->C, (long long)start_pos + sh->C);
+  return PF_OK;
+}
+
+pf_status pf_dense_workspace_bytes(const pf_shape* sh, int64_t* bytes) {
+  if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
+  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  const int P = sm_count();
+  if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
+  *bytes = dense_workspace_bytes(sh->d, P);
+  return PF_OK;
+}
+
+pf_status pf_attn_dense(const pf_shape* sh, const void* q, const void* k_hist, const void* v_hist,
+                        const void* k_chunk, const void* v_chunk, const void* mask,
+                        int32_t start_pos, void* out, float* lse, void* out_k, void* out_v,
+                        void* workspace, int64_t workspace_bytes, void* stream) {
+  return dense_entry(sh, q, k_hist, v_hist, k_chunk, v_chunk, mask, nullptr, start_pos, out, lse, out_k,
+                     out_v, workspace, workspace_bytes, stream);
+}
+
+pf_status pf_attn_indexed(const pf_shape* sh, const void* q, const void* k_hist, const void* v_hist,
+                          const void* k_chunk, const void* v_chunk, const int32_t* keep_idx,
+                          const int32_t* keep_cnt, int32_t keep_stride, int32_t ratio, int32_t start_pos,
+                          void* out, float* lse, void* out_k, void* out_v, void* workspace,
+                          int64_t workspace_bytes, void* stream) {
+  const IndexSel isel{keep_idx, keep_cnt, keep_stride, ratio};
+  return dense_entry(sh, q, k_hist, v_hist, k_chunk, v_chunk, nullptr, &isel, start_pos, out, lse, out_k,
+                     out_v, workspace, workspace_bytes, stream);
+}
+
+pf_status pf_indexed_workspace_bytes(const pf_shape* sh, int32_t start_pos, int64_t* bytes) {
+  return pf_dense_workspace_bytes_masked(sh, start_pos, bytes);
 }
 
 pf_status pf_sparse_query_sizes(const pf_shape* sh, int32_t start_pos, int32_t block,

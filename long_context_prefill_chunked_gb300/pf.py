@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "PF_OK", 1: "PF_EINVAL", 2: "PF_EUNSUPPORTED", 3: "PF_ECUDA",
                 5: "PF_ERANGE"}
 
 EXPORTS = ["pf_attn_dense", "pf_dense_workspace_bytes", "pf_dense_workspace_bytes_masked",
+           "pf_attn_indexed", "pf_indexed_workspace_bytes",
            "pf_block_index", "pf_attn_sparse",
            "pf_sparse_query_sizes",
            "pf_stream_status", "pf_set_wait_timeout", "pf_set_debug_withhold", "pf_launch_count",
@@ -86,6 +87,8 @@ def load() -> ctypes.CDLL:
     lib.pf_attn_dense.argtypes = [P(Shape), V, V, V, V, V, V, I32, V, V, V, V, V, I64, V]
     lib.pf_dense_workspace_bytes.argtypes = [P(Shape), P(I64)]
     lib.pf_dense_workspace_bytes_masked.argtypes = [P(Shape), I32, P(I64)]
+    lib.pf_attn_indexed.argtypes = [P(Shape), V, V, V, V, V, V, V, I32, I32, I32, V, V, V, V, V, I64, V]
+    lib.pf_indexed_workspace_bytes.argtypes = [P(Shape), I32, P(I64)]
     lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(KeepRules), P(Sel), V]
     lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V, V]
     lib.pf_sparse_query_sizes.argtypes = [P(Shape), I32, I32, P(SparseSizes)]
@@ -99,6 +102,7 @@ def load() -> ctypes.CDLL:
     lib.pf_last_error.restype = ctypes.c_char_p
     lib.pf_version.restype = ctypes.c_char_p
     for name in ("pf_attn_dense", "pf_dense_workspace_bytes", "pf_dense_workspace_bytes_masked",
+                 "pf_attn_indexed", "pf_indexed_workspace_bytes",
                  "pf_block_index", "pf_attn_sparse",
                  "pf_sparse_query_sizes", "pf_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
@@ -180,8 +184,8 @@ _WORKSPACES = {}
 
 def dense_workspace(q, stream=None, masked_start_pos=None) -> torch.Tensor:
     """The pf_attn_dense workspace (tail split; with masked_start_pos, also the packed bits of
-    an explicit mask) for q, one per (device, stream) so that calls on different streams never
-    share one."""
+    an explicit mask or of pf_attn_indexed's keep lists, whose workspace has the same size) for
+    q, one per (device, stream) so that calls on different streams never share one."""
     lib = load()
     sh = Shape()
     sh.d = q.shape[-1]
@@ -207,6 +211,35 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
     uses a cached per-(device, stream) buffer (tail split on), None runs every unit whole,
     or a caller-owned uint8 tensor of at least pf_dense_workspace_bytes.  lse: an optional
     fp32 [B, Hq, C] tensor that receives log sum_j exp(l_j) per row."""
+    return _dense_call(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask, None, out, out_k, out_v,
+                       out_dtype, scale, stream, workspace, lse)
+
+
+def attn_indexed(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, keep_idx, keep_cnt, ratio, out=None,
+                 out_k=None, out_v=None, out_dtype=torch.float32, scale=0.0, stream=None, workspace=True,
+                 lse=None):
+    """Index-driven attention (pf_attn_indexed): row i attends to the keys of its kept compressed
+    blocks (keep_idx [C, S] int32, the first keep_cnt[i] entries of row i; block c covers keys
+    ratio*c .. ratio*c + ratio - 1) plus the keys after its last complete block.  workspace:
+    True (a cached buffer) or a caller-owned uint8 tensor of at least
+    pf_indexed_workspace_bytes; the call needs one."""
+    if workspace is None or workspace is False:
+        raise ValueError("attn_indexed needs a workspace")
+    C = q.shape[1] if q.dim() == 4 else -1
+    if keep_idx.dim() != 2 or keep_idx.shape[0] != C or keep_idx.dtype != torch.int32 or \
+            keep_idx.stride(1) != 1:
+        raise ValueError("keep_idx must be an int32 [C, S] tensor with contiguous rows")
+    _expect(keep_cnt, (C,), "keep_cnt", q.device)
+    _expect(keep_idx, tuple(keep_idx.shape), "keep_idx", q.device)
+    if keep_cnt.dtype != torch.int32 or not keep_cnt.is_contiguous():
+        raise ValueError("keep_cnt must be a contiguous int32 [C] tensor")
+    keep = (keep_idx, keep_cnt, int(keep_idx.stride(0)), int(ratio))
+    return _dense_call(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, None, keep, out, out_k, out_v,
+                       out_dtype, scale, stream, workspace, lse)
+
+
+def _dense_call(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask, keep, out, out_k, out_v, out_dtype,
+                scale, stream, workspace, lse):
     lib = load()
     if q.dim() != 4:
         raise ValueError("q must be [B, C, Hq, d]")
@@ -230,7 +263,7 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
         _expect(mask, (C, start_pos + C), "mask", dev)
     _expect_lse(lse, B, Hq, C, dev)
     if workspace is True:
-        workspace = dense_workspace(q, stream, None if mask is None else start_pos)
+        workspace = dense_workspace(q, stream, None if mask is None and keep is None else start_pos)
     elif workspace is False:
         workspace = None
     if workspace is not None and workspace.device != dev:
@@ -254,10 +287,18 @@ def attn_dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, out=No
             raise ValueError("mask must be [C, start_pos + C] with contiguous rows")
         sh.mask_dtype = _dtype(mask)
         sh.mask_ld = mask.stride(0)
-    _check(lib.pf_attn_dense(ctypes.byref(sh), _ptr(q), _ptr(k_hist if start_pos > 0 else None),
-                             _ptr(v_hist if start_pos > 0 else None), _ptr(k_chunk), _ptr(v_chunk),
-                             _ptr(mask), int(start_pos), _ptr(out), _ptr(lse), _ptr(out_k),
-                             _ptr(out_v), _ptr(workspace), int(ws_bytes), _stream(stream)))
+    kh = _ptr(k_hist if start_pos > 0 else None)
+    vh = _ptr(v_hist if start_pos > 0 else None)
+    if keep is None:
+        _check(lib.pf_attn_dense(ctypes.byref(sh), _ptr(q), kh, vh, _ptr(k_chunk), _ptr(v_chunk),
+                                 _ptr(mask), int(start_pos), _ptr(out), _ptr(lse), _ptr(out_k),
+                                 _ptr(out_v), _ptr(workspace), int(ws_bytes), _stream(stream)))
+    else:
+        keep_idx, keep_cnt, stride, ratio = keep
+        _check(lib.pf_attn_indexed(ctypes.byref(sh), _ptr(q), kh, vh, _ptr(k_chunk), _ptr(v_chunk),
+                                   _ptr(keep_idx), _ptr(keep_cnt), stride, ratio, int(start_pos),
+                                   _ptr(out), _ptr(lse), _ptr(out_k), _ptr(out_v), _ptr(workspace),
+                                   int(ws_bytes), _stream(stream)))
     return out
 
 

@@ -82,6 +82,24 @@ def test_dense_rejects_bad_arguments(lib):
     assert dense(lib, bad) == pf.PF_EINVAL
 
 
+def indexed(lib, sh, keep_idx=FAKE, keep_cnt=FAKE, stride=16, ratio=4, s=0, ws=FAKE, ws_bytes=1 << 30):
+    return lib.pf_attn_indexed(ctypes.byref(sh), FAKE, None, None, FAKE, FAKE, keep_idx, keep_cnt, stride,
+                               ratio, s, FAKE, None, None, None, ws, ws_bytes, None)
+
+
+def test_indexed_rejects_bad_arguments(lib):
+    sh = shape()
+    assert indexed(lib, sh, ratio=0) == pf.PF_EINVAL
+    assert indexed(lib, sh, ratio=129) == pf.PF_EINVAL
+    assert indexed(lib, sh, keep_cnt=None) == pf.PF_EINVAL
+    assert indexed(lib, sh, keep_idx=None) == pf.PF_EINVAL                  # entries but no list
+    assert indexed(lib, sh, stride=-1) == pf.PF_EINVAL
+    assert indexed(lib, sh, keep_idx=ctypes.c_void_p(0x100002)) == pf.PF_EINVAL
+    assert indexed(lib, sh, ws=None) == pf.PF_EINVAL                        # the bits need a workspace
+    assert indexed(lib, shape(C=(1 << 20) + 128)) == pf.PF_EUNSUPPORTED     # past 2^20 keys
+    assert b"1048576" in lib.pf_last_error()
+
+
 def test_sparse_rejects_bad_arguments(lib):
     sel = pf.Sel(0x100000, 0x100000, 0x100000, 0x100000)
     sh = shape()
