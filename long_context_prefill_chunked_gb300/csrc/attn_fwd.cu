@@ -535,13 +535,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (c > r) x[c] = -INFINITY;
         }
       } else if (MODE == MODE_MASKB) {
-        // bit set = kept (value 0); dropped keys (and keys past T, whose bits are 0) are -inf
+        // bit set = kept (value 0); dropped keys (and keys past T, whose bits are 0) are -inf;
+        // a word of 32 kept keys (most words of a causal-like mask) needs no selects
         const uint32_t wq[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
+          if (wq[q] != 0xffffffffu) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (!((wq[q] >> i) & 1u)) x[32 * q + i] = -INFINITY;
+            for (int i = 0; i < 32; ++i)
+              if (!((wq[q] >> i) & 1u)) x[32 * q + i] = -INFINITY;
+          }
       } else if (MODE == MODE_MASK) {
         xs = 1.f;
         const int key0 = (j0 + j) * kTile;
