@@ -206,8 +206,23 @@ def run_case(args):
     __graft_entry__.build()
     import long_context_prefill_chunked_gb300 as pfx
     import prefill_inputs as pi
-    w = pi.config(5 if args.case == "sparse-128k-chunk" else 4)
     to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    if args.case in ("indexed-config3", "mask-config3"):
+        # a 4096-row chunk over an 8192-token history (16q/8kv, d128), 512 compressed blocks of
+        # 4 keys kept per query: as keep lists, or folded into an fp32 0 / -30000 mask
+        w3 = pi.config(3)
+        s = 8192
+        q, kh, vh, kc, vc = (to_dev(x) for x in w3.chunk_views(s))
+        mask, kept = pi.indexer_fold_mask(w3.seed, w3.chunk, s)
+        if args.case == "indexed-config3":
+            idx = torch.from_numpy(np.stack(kept).astype(np.int32)).cuda()
+            cnt = torch.full((w3.chunk,), idx.shape[1], dtype=torch.int32, device="cuda")
+            run = lambda: pfx.attn_indexed(q, kh, vh, kc, vc, s, idx, cnt, 4)
+        else:
+            m = torch.from_numpy(mask).cuda()
+            run = lambda: pfx.attn_dense(q, kh, vh, kc, vc, s, mask=m)
+        return _time_case(args, pfx, run, 4.0 * w3.Hq * w3.d * (w3.chunk * s + w3.chunk * (w3.chunk + 1) // 2), s)
+    w = pi.config(5 if args.case == "sparse-128k-chunk" else 4)
     if args.case == "sparse-128k-chunk":
         # the last 4096-row chunk of the 128K planted prompt: selection and block-sparse
         # attention against a 131072-key history (K/V 268 MB each, beyond L2)
@@ -271,10 +286,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse", "sparse-128k-chunk"],
+    ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse", "sparse-128k-chunk",
+                                                       "indexed-config3", "mask-config3"],
                     help="profiling cases, timings only: dense-chunk (one 4096-row chunk at "
                          "--start), sparse (the 32K block-sparse pair), sparse-128k-chunk (the "
-                         "pair for the last 4096-row chunk of the 128K prompt)")
+                         "pair for the last 4096-row chunk of the 128K prompt), indexed-config3 / "
+                         "mask-config3 (config 3's selection as keep lists / as a folded mask)")
     ap.add_argument("--start", type=int, default=N_TOK - CHUNK,
                     help="dense-chunk case: the chunk's first token (a multiple of 4096)")
     args = ap.parse_args()
