@@ -160,3 +160,28 @@ def test_binding_refuses_mismatched_extents(lib):
     k_all = torch.zeros((B, s + C, Hkv, d), dtype=bf)
     with pytest.raises(ValueError, match="k"):
         pf.block_index(q, k_all[:, :C], s)
+
+
+def test_binding_refuses_bad_keep_lists(lib):
+    """attn_indexed: the keep lists must be int32 [C, S] with contiguous rows and keep_cnt an
+    int32 [C] tensor, and a workspace is required (all raise before any library call)."""
+    import torch
+    B, C, Hq, Hkv, d, s = 1, 256, 4, 2, 128, 128
+    bf = torch.bfloat16
+    q = torch.zeros((B, C, Hq, d), dtype=bf)
+    kc = torch.zeros((B, C, Hkv, d), dtype=bf)
+    kh = torch.zeros((B, s, Hkv, d), dtype=bf)
+    idx = torch.zeros((C, 8), dtype=torch.int32)
+    cnt = torch.zeros((C,), dtype=torch.int32)
+    with pytest.raises(ValueError, match="keep_idx"):
+        pf.attn_indexed(q, kh, kh, kc, kc, s, idx.long(), cnt, 4)
+    with pytest.raises(ValueError, match="keep_idx"):
+        pf.attn_indexed(q, kh, kh, kc, kc, s, idx[:128], cnt, 4)
+    with pytest.raises(ValueError, match="keep_idx"):
+        pf.attn_indexed(q, kh, kh, kc, kc, s, idx.t().contiguous().t(), cnt, 4)
+    with pytest.raises(ValueError, match="keep_cnt"):
+        pf.attn_indexed(q, kh, kh, kc, kc, s, idx, cnt[:100], 4)
+    with pytest.raises(ValueError, match="keep_cnt"):
+        pf.attn_indexed(q, kh, kh, kc, kc, s, idx, cnt.long(), 4)
+    with pytest.raises(ValueError, match="workspace"):
+        pf.attn_indexed(q, kh, kh, kc, kc, s, idx, cnt, 4, workspace=None)
