@@ -874,13 +874,10 @@ __global__ void kv_relayout_kernel(const uint16_t* __restrict__ src, uint16_t* _
 
 template <int MODE>
 cudaError_t launch_mode(const AttnMaps& maps, const AttnArgs& a, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SM_ALLOC);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<int> configured[64];
+  cudaError_t e =
+      ensure_dynamic_smem(reinterpret_cast<const void*>(attn_fwd_kernel<MODE>), SM_ALLOC, configured);
+  if (e != cudaSuccess) return e;
   const int units = a.n_qt * a.n_hp * a.B;
   const int grid = a.n_whole + (units - a.n_whole) * a.split_k;
   attn_fwd_kernel<MODE><<<grid, kAttnThreads, SM_ALLOC, st>>>(maps, a);

@@ -363,13 +363,10 @@ cudaError_t launch_share_group(const IndexArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         X_ALLOC);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<int> configured[64];
+  cudaError_t e =
+      ensure_dynamic_smem(reinterpret_cast<const void*>(index_tc_kernel), X_ALLOC, configured);
+  if (e != cudaSuccess) return e;
   const int grid = a.n_qt * a.n_hp * a.B;
   index_tc_kernel<<<grid, kIndexThreads, X_ALLOC, st>>>(maps, a);
   ++t_launches;

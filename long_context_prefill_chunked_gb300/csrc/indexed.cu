@@ -81,12 +81,11 @@ cudaError_t launch_index_pack(const int32_t* keep_idx, const int32_t* keep_cnt, 
                               int ratio, int C, int s, uint32_t* bits, int words, uint32_t* tiles,
                               int tile_words, unsigned* status, cudaStream_t st) {
   const size_t smem = (size_t)words * 4;
-  static size_t configured = 48 * 1024;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(index_pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+  static std::atomic<int> configured[64];
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(index_pack_kernel), (int)smem, configured);
     if (e != cudaSuccess) return e;
-    configured = smem;
   }
   const int grid = C < 152 * 8 ? C : 152 * 8;
   index_pack_kernel<<<grid, 256, smem, st>>>(keep_idx, keep_cnt, stride, ratio, C, s, bits, words, tiles,

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pf {
 
 constexpr int kTile = 128;        // query rows and keys per tile (= key block of the sparse path)
@@ -126,5 +128,19 @@ cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t
 cudaError_t launch_share_group(const IndexArgs& a, cudaStream_t st);
 
 extern thread_local long long t_launches;
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device once: the
+// attribute belongs to each device's copy of the kernel, so `done` holds the limit set so far
+// per device (64 entries, zero-initialised).
+inline cudaError_t ensure_dynamic_smem(const void* kernel, int bytes, std::atomic<int>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(bytes, std::memory_order_relaxed);
+  return e;
+}
 
 }  // namespace pf
