@@ -230,7 +230,8 @@ def attn_indexed(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, keep_idx, keep_
             keep_idx.stride(1) != 1:
         raise ValueError("keep_idx must be an int32 [C, S] tensor with contiguous rows")
     _expect(keep_cnt, (C,), "keep_cnt", q.device)
-    _expect(keep_idx, tuple(keep_idx.shape), "keep_idx", q.device)
+    if keep_idx.device != q.device:
+        raise ValueError("keep_idx is on %s, expected %s" % (keep_idx.device, q.device))
     if keep_cnt.dtype != torch.int32 or not keep_cnt.is_contiguous():
         raise ValueError("keep_cnt must be a contiguous int32 [C] tensor")
     keep = (keep_idx, keep_cnt, int(keep_idx.stride(0)), int(ratio))
