@@ -185,3 +185,47 @@ def test_binding_refuses_bad_keep_lists(lib):
         pf.attn_indexed(q, kh, kh, kc, kc, s, idx, cnt.long(), 4)
     with pytest.raises(ValueError, match="workspace"):
         pf.attn_indexed(q, kh, kh, kc, kc, s, idx, cnt, 4, workspace=None)
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "pf.h"
+
+int main(void) {
+  pf_shape sh;
+  memset(&sh, 0, sizeof(sh));
+  sh.B = 1; sh.Hq = 4; sh.Hkv = 2; sh.d = 128; sh.C = 256;
+  sh.in_dtype = PF_BF16; sh.out_dtype = PF_F32; sh.mask_dtype = PF_F32;
+  void* fake = (void*)0x100000;
+  int32_t cnt = 0;
+  if (strstr(pf_version(), "sm_103a") == NULL) return 1;
+  if (pf_attn_dense(NULL, fake, NULL, NULL, fake, fake, NULL, 0, fake, NULL, NULL, NULL, NULL, 0, NULL)
+      != PF_EINVAL) return 2;
+  if (pf_attn_indexed(&sh, fake, NULL, NULL, fake, fake, (const int32_t*)fake, &cnt, 8, 0, 0, fake, NULL,
+                      NULL, NULL, fake, 1, NULL) != PF_EINVAL) return 3;
+  if (pf_last_error()[0] == '\0') return 4;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/pf.h compiles as C99 with warnings as errors, and a C program linked against
+    libpf.so reaches the validation paths (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    libdir = os.path.dirname(pf.LIB_PATH)
+    exe = tmp_path / "caller"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lpf", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
