@@ -168,6 +168,28 @@ def _blas_threads():
         return os.cpu_count()
 
 
+def host_cpu():
+    """The host CPU as /proc/cpuinfo names it (x86 'model name', Arm implementer and part),
+    with the architecture; the oracle's timing is only meaningful beside it."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ":" in ln:
+                    k, v = ln.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        model = fields["model name"]
+    elif "CPU part" in fields:
+        model = "implementer %s part %s" % (fields.get("CPU implementer", "?"), fields["CPU part"])
+    else:
+        model = platform.processor() or "unknown"
+    return "%s (%s, %d logical cores)" % (model, platform.machine(), os.cpu_count() or 0)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -188,7 +210,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "config": {"workload": WORKLOAD % pi.PLANT_BETA},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": per_step[0][1]["threads"],
-                         "kind": "oracle",
+                         "kind": "oracle", "host": host_cpu(),
                          "sample": "%d query rows x 32 heads (half from the last dense chunk, half "
                                    "block-sparse), float64 numpy oracle" % rows},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -498,6 +520,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, det = oracle_sample_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": det["threads"], "kind": "oracle",
+                                "host": host_cpu(),
                                 "sample": "%d query rows x 32 heads in %.1f s: half from the last dense "
                                           "chunk (keys 28672..32767), half block-sparse; float64 numpy "
                                           "oracle" % (det["rows"], det["seconds"])}

@@ -31,7 +31,7 @@ def test_reference_arm_prints_one_contract_line(monkeypatch):
     assert "32K" in line["config"]["workload"]
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
-    assert "query rows" in cb["sample"]
+    assert "query rows" in cb["sample"] and "cores" in cb["host"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
