@@ -253,6 +253,17 @@ def test_indexed_visible_count(ratio):
         assert np.array_equal(oracle.indexed_visible_keys(p, dup, ratio), vis)
 
 
+def test_indexed_negative_control():
+    """The pages' check that was not sensitive enough: a causal-only run must differ from the
+    selection by far more than the parity tolerance, or a test comparing them proves nothing."""
+    s, C, ratio, nk = 512, 32, 4, 16
+    q, kh, vh, kc, vc = rand_case(19, B=1, Hq=2, Hkv=1, C=C, s=s, d=32)
+    _, kept = pi.indexer_fold_mask(20, C, s, kept_blocks=nk, ratio=ratio)
+    sel = oracle.dense_indexed(q, kh, vh, kc, vc, s, kept, ratio)
+    causal = oracle.dense(q, kh, vh, kc, vc, s)
+    assert np.max(np.abs(sel - causal)) >= 10 * 5e-3
+
+
 def test_indexed_rejects_a_bad_selection():
     with pytest.raises(ValueError):
         oracle.indexed_visible_keys(10, [2], 4)       # block 2 holds keys 8..11: not complete at 10
