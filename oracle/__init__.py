@@ -6,8 +6,9 @@ library and never calls it.
 """
 from .attention import (MASK_DROP, KeepRules, Selection, block_counts, block_select,
                         causal_additive, chunk_kv_cache_layout, dense, dense_indexed,
-                        indexed_visible_keys, pool_blocks, skip_share, sparse, tile_union)
+                        indexed_visible_keys, pool_blocks, skip_share, sparse, sparse_for_selection,
+                        tile_union)
 
 __all__ = ["MASK_DROP", "KeepRules", "Selection", "block_counts", "block_select", "causal_additive",
            "chunk_kv_cache_layout", "dense", "dense_indexed", "indexed_visible_keys", "pool_blocks",
-           "skip_share", "sparse", "tile_union"]
+           "skip_share", "sparse", "sparse_for_selection", "tile_union"]

@@ -9,7 +9,11 @@ numpy arrays (exact upcasts of the fp16/bf16 inputs).
 Each function is the plain definition written out, row by row, with a numpy
 matmul as the only library step: no tiling, no online softmax, no fusion.
 Rows are computed in groups only to bound memory; every row's result depends
-on that row alone.
+on that row alone.  The block-sparse function groups rows by their diagonal
+block and takes a group's logits on the keys of the blocks some row of the
+group keeps, a superset of each row's exact keys; every other key of a row is
+masked to exp(-inf) = 0 exactly, so the grouping changes no row's value beyond
+float64 summation order.
 
 Sources (page title, section):
   * "Flash attention on ANE: fast long-context prefill", section
@@ -106,19 +110,30 @@ def dense(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask=None, scale=None,
     out = np.empty((B, len(rows), len(heads), d))
     lse = np.empty((B, len(rows), len(heads)))
     step = max(1, _ROW_ELEMS // T)
+    jc = np.arange(C)[None, :]
     for b in range(B):
-        for hi, h in enumerate(heads):
-            g = h // G
-            kg, vg = k[b, :, g, :], v[b, :, g, :]
-            for r0 in range(0, len(rows), step):
-                rr = rows[r0:r0 + step]
-                logits = (q[b, rr, h, :] @ kg.T) * scale
-                logits += causal_additive(C, s, rr) if mask is None else mask[rr, :]
-                m = logits.max(axis=1, keepdims=True)
-                w = np.exp(logits - m)
-                den = w.sum(axis=1, keepdims=True)
-                out[b, r0:r0 + len(rr), hi, :] = (w @ vg) / den
-                lse[b, r0:r0 + len(rr), hi] = m[:, 0] + np.log(den[:, 0])
+        for g in sorted({h // G for h in heads}):
+            kg = np.ascontiguousarray(k[b, :, g, :])
+            vg = np.ascontiguousarray(v[b, :, g, :])
+            for hi, h in enumerate(heads):
+                if h // G != g:
+                    continue
+                for r0 in range(0, len(rows), step):
+                    rr = rows[r0:r0 + step]
+                    logits = q[b, rr, h, :] @ kg.T
+                    logits *= scale
+                    if mask is None:
+                        # causal: every history key (j < s) is visible; chunk key s + c gets
+                        # -30000 where c > i (the columns below s would add 0)
+                        logits[:, s:] += np.where(jc <= rr[:, None], 0.0, MASK_DROP)
+                    else:
+                        logits += mask[rr, :]
+                    m = logits.max(axis=1, keepdims=True)
+                    logits -= m
+                    np.exp(logits, out=logits)
+                    den = logits.sum(axis=1, keepdims=True)
+                    out[b, r0:r0 + len(rr), hi, :] = (logits @ vg) / den
+                    lse[b, r0:r0 + len(rr), hi] = m[:, 0] + np.log(den[:, 0])
     return (out, lse) if with_lse else out
 
 
@@ -219,6 +234,10 @@ class Selection:
     heads: list
     start_pos: int
     block: int
+    # bool [B, R, Hsel, nblk]: the candidate's probability ratio exp(s_ib - s_max) lies within
+    # 1e-4 relative of alpha, so float rounding may decide it either way (propagated through
+    # the keep rules' group unions like ``near``); near = near_pairs.any(-1)
+    near_pairs: np.ndarray = None
 
 
 @dataclasses.dataclass(frozen=True)
@@ -266,7 +285,7 @@ def block_select(q, k, start_pos, block, alpha, scale=None, rows=None, heads=Non
     ob = (s + rows) // block                                   # [R]
     cand = np.arange(nblk)[None, :] < ob[:, None]              # [R, nblk]
     kept = np.zeros((B, len(rows), len(heads), nblk), dtype=bool)
-    near = np.zeros((B, len(rows), len(heads)), dtype=bool)
+    near_pairs = np.zeros((B, len(rows), len(heads), nblk), dtype=bool)
     scores = np.empty((B, len(rows), len(heads), nblk))
     for b in range(B):
         for hi, h in enumerate(heads):
@@ -285,8 +304,8 @@ def block_select(q, k, start_pos, block, alpha, scale=None, rows=None, heads=Non
             keep[np.arange(len(rows)), ob] = True
             kept[b, :, hi] = keep
             if alpha > 0:
-                near[b, :, hi] = (cand & (np.abs(ratio - alpha) <= near_rel * alpha)).any(axis=1)
-    return Selection(kbar, kept, near, scores, rows, heads, s, block)
+                near_pairs[b, :, hi] = cand & (np.abs(ratio - alpha) <= near_rel * alpha)
+    return Selection(kbar, kept, near_pairs.any(axis=-1), scores, rows, heads, s, block, near_pairs)
 
 
 def _select_grouped(q, k, start_pos, block, alpha, scale, rows, heads, near_rel, rules):
@@ -302,7 +321,7 @@ def _select_grouped(q, k, start_pos, block, alpha, scale, rows, heads, near_rel,
     all_heads = list(range(Hq))
     base_rules = dataclasses.replace(rules, row_group=1, share_kv_group=False)
     full = block_select(q, k, s, block, alpha, scale, all_rows, all_heads, near_rel, base_rules)
-    kept, near = full.kept.copy(), full.near.copy()
+    kept, near_pairs = full.kept.copy(), full.near_pairs.copy()
     ob = (s + all_rows) // block
     cand = np.arange(kept.shape[-1])[None, :] < ob[:, None]
     if g_rows > 1:
@@ -311,16 +330,17 @@ def _select_grouped(q, k, start_pos, block, alpha, scale, rows, heads, near_rel,
             m = grp == gi
             u = kept[:, m].any(axis=1, keepdims=True)              # [B, 1, Hq, nblk]
             kept[:, m] |= u & cand[m][None, :, None, :]
-            near[:, m] |= near[:, m].any(axis=1, keepdims=True)
+            near_pairs[:, m] |= near_pairs[:, m].any(axis=1, keepdims=True)
     if rules.share_kv_group:
         for g in range(Hq // G):
             hs = slice(g * G, (g + 1) * G)
             u = kept[:, :, hs].any(axis=2, keepdims=True)
             kept[:, :, hs] |= u
-            near[:, :, hs] |= near[:, :, hs].any(axis=2, keepdims=True)
+            near_pairs[:, :, hs] |= near_pairs[:, :, hs].any(axis=2, keepdims=True)
     hi = np.array(heads)
-    return Selection(full.kbar, kept[:, rows][:, :, hi], near[:, rows][:, :, hi],
-                     full.scores[:, rows][:, :, hi], rows, heads, s, block)
+    np_sel = near_pairs[:, rows][:, :, hi]
+    return Selection(full.kbar, kept[:, rows][:, :, hi], np_sel.any(axis=-1),
+                     full.scores[:, rows][:, :, hi], rows, heads, s, block, np_sel)
 
 
 def tile_union(kept_tile_rows) -> np.ndarray:
@@ -360,27 +380,43 @@ def sparse(q, k, v, start_pos, block, alpha, scale=None, rows=None, heads=None, 
     lse = np.empty((B, len(rows), len(heads)))
     p_all = s + rows
     ob_all = p_all // block
-    jblk = np.arange(T) // block
+    bidx = np.arange(nblk)[None, :]
     step = max(1, _ROW_ELEMS // T)
     for b in range(B):
-        for hi, h in enumerate(heads):
-            g = h // G
-            kg, vg = k[b, :, g, :], v[b, :, g, :]
-            for r0 in range(0, len(rows), step):
-                sl = slice(r0, r0 + step)
-                rr, p, ob = rows[sl], p_all[sl], ob_all[sl]
-                keep = sel.kept[b, sl, hi]                                   # [r, nblk]
-                exact = keep[:, jblk] & (np.arange(T)[None, :] <= p[:, None])
-                skipped = (np.arange(nblk)[None, :] < ob[:, None]) & ~keep
-                logits = np.where(exact, (q[b, rr, h, :] @ kg.T) * scale, -np.inf)
-                pooled = np.where(skipped, sel.scores[b, sl, hi], -np.inf)
-                m = np.maximum(logits.max(axis=1), pooled.max(axis=1))[:, None]
-                we = np.exp(logits - m)
-                wp = nb[None, :] * np.exp(pooled - m)
-                num = we @ vg + wp @ vbar[b, g]
-                den = we.sum(axis=1) + wp.sum(axis=1)
-                out[b, sl, hi, :] = num / den[:, None]
-                lse[b, sl, hi] = m[:, 0] + np.log(den)
+        for g in sorted({h // G for h in heads}):
+            kg = np.ascontiguousarray(k[b, :, g, :])
+            vg = np.ascontiguousarray(v[b, :, g, :])
+            his = [hi for hi, h in enumerate(heads) if h // G == g]
+            # rows sharing a diagonal block share their candidates; a group's logits are taken
+            # on the keys of the blocks some row of the group keeps for some head of this KV
+            # head (a superset of every row's exact keys E_i), and each row masks the rest to
+            # exp(-inf) = 0
+            for obv in np.unique(ob_all):
+                grp = np.flatnonzero(ob_all == obv)
+                for r0 in range(0, len(grp), step):
+                    sl = grp[r0:r0 + step]
+                    rr, p = rows[sl], p_all[sl]
+                    blocks = np.flatnonzero(sel.kept[b][sl][:, his].any(axis=(0, 1)))
+                    if 2 * len(blocks) > nblk:
+                        keys, ks, vs = np.arange(T), kg, vg
+                    else:
+                        keys = (blocks[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+                        keys = keys[keys < T]
+                        ks, vs = kg[keys], vg[keys]
+                    for hi in his:
+                        h = heads[hi]
+                        keep = sel.kept[b, sl, hi]                               # [r, nblk]
+                        exact = keep[:, keys // block] & (keys[None, :] <= p[:, None])
+                        skipped = (bidx < obv) & ~keep
+                        logits = np.where(exact, (q[b, rr, h, :] @ ks.T) * scale, -np.inf)
+                        pooled = np.where(skipped, sel.scores[b, sl, hi], -np.inf)
+                        m = np.maximum(logits.max(axis=1), pooled.max(axis=1))[:, None]
+                        we = np.exp(logits - m)
+                        wp = nb[None, :] * np.exp(pooled - m)
+                        num = we @ vs + wp @ vbar[b, g]
+                        den = we.sum(axis=1) + wp.sum(axis=1)
+                        out[b, sl, hi, :] = num / den[:, None]
+                        lse[b, sl, hi] = m[:, 0] + np.log(den)
     return (out, sel, lse) if with_lse else (out, sel)
 
 
@@ -394,3 +430,39 @@ def skip_share(sel: Selection) -> float:
         return 0.0
     kept_cand = (sel.kept & cand[None, :, None, :]).sum()
     return float(1.0 - kept_cand / n_cand)
+
+
+def sparse_for_selection(q, k, v, start_pos, block, alpha, kept, scale=None, rows=None, heads=None,
+                         rules=None, with_lse=False):
+    """Expected block-sparse output for a selection taken with finite-precision scores.
+
+    A pair (row, block) whose probability ratio exp(s_ib - s_max) lies within 1e-4
+    relative of alpha may be decided either way by rounding; any other pair is fixed
+    by the definition (``block_select``).  ``kept`` (bool [B, R, Hsel, nblk]) must
+    therefore equal the definition's selection outside those near pairs, else
+    ValueError.  Returns (out, sel, flipped): out is the definition's output for each
+    row under ``kept`` (rows that decided no near pair differently take the plain
+    ``sparse`` result), sel the definition's selection, flipped the indices of the
+    rows whose selection differs; with with_lse also the log of each row's
+    denominator under ``kept``.
+    """
+    sel = block_select(q, k, start_pos, block, alpha, scale, rows, heads, rules=rules)
+    kept = np.asarray(kept, dtype=bool)
+    if kept.shape != sel.kept.shape:
+        raise ValueError("kept has shape %s, expected %s" % (kept.shape, sel.kept.shape))
+    diff = kept != sel.kept
+    bad = diff & ~sel.near_pairs
+    if bad.any():
+        b, r, h, blk = (int(x[0]) for x in np.nonzero(bad))
+        raise ValueError("selection differs from the definition at a pair outside the threshold band "
+                         "(batch %d, row %d, head %d, block %d; %d such pairs)"
+                         % (b, int(sel.rows[r]), sel.heads[h], blk, int(bad.sum())))
+    out, _, lse = sparse(q, k, v, start_pos, block, alpha, scale, sel=sel, with_lse=True)
+    flipped = np.flatnonzero(diff.any(axis=(0, 2, 3)))
+    if flipped.size:
+        alt = Selection(sel.kbar, kept[:, flipped], sel.near[:, flipped], sel.scores[:, flipped],
+                        sel.rows[flipped], sel.heads, sel.start_pos, sel.block, sel.near_pairs[:, flipped])
+        o_alt, _, l_alt = sparse(q, k, v, start_pos, block, alpha, scale, sel=alt, with_lse=True)
+        out[:, flipped] = o_alt
+        lse[:, flipped] = l_alt
+    return (out, sel, flipped, lse) if with_lse else (out, sel, flipped)

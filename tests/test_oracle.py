@@ -575,3 +575,101 @@ def test_dense_tail_rows_equal_dense_attention():
     dense = oracle.dense(q, k[:, :s], v[:, :s], k[:, s:], v[:, s:], s)
     assert np.max(np.abs(out[0, N - 16:] - dense[0, N - 16:])) <= 1e-12
     assert np.max(np.abs(out[0, :N - 16] - dense[0, :N - 16])) > 1e-6    # the rest is sparse
+
+
+# --------------------------------------------------------------------------
+# the near-threshold band: pairs whose probability ratio sits within 1e-4 relative of alpha
+# --------------------------------------------------------------------------
+def _band_case(eps, alpha=0.1, t3=10.0, spread=0.0):
+    """Four 2-token blocks of keys (t_b, 0, 0, 0), query (1, 0, 0, 0), scale 1, so the pooled
+    logit of block b is exactly t_b.  Rows 6 and 7 (block 3) have candidates 0, 1, 2:
+    t_0 = 0 is the hottest candidate, t_1 = ln(alpha (1 + eps)) puts block 1's probability
+    ratio at alpha (1 + eps), t_2 = -5 is far below the threshold; the diagonal block 3 has
+    t_3 (default 10, above every candidate: it must not enter the row maximum).  Rows 4 and 5
+    (block 2) have candidates 0 and 1 against the same maximum.  With spread, the keys of
+    every block alternate t_b + spread, t_b - spread (the block mean stays t_b)."""
+    t = [0.0, math.log(alpha * (1.0 + eps)), -5.0, t3]
+    N, blk, d = 8, 2, 4
+    q = np.zeros((1, N, 1, d))
+    q[0, :, 0, 0] = 1.0
+    k = np.zeros((1, N, 1, d))
+    v = np.zeros((1, N, 1, d))
+    for j in range(N):
+        k[0, j, 0, 0] = t[j // blk] + (spread if j % 2 == 0 else -spread)
+        v[0, j, 0] = (1.0, j, (j % 2) - 0.5, j // blk)
+    return q, k, v, blk, t
+
+
+@pytest.mark.parametrize("eps", [5e-5, -5e-5, 9e-5, -9e-5])
+def test_near_band_flags_a_pair_inside(eps):
+    q, k, v, blk, _ = _band_case(eps)
+    sel = oracle.block_select(q, k, 0, blk, 0.1, scale=1.0)
+    for r in (4, 5, 6, 7):                           # blocks 2 and 3: block 1 is a candidate
+        assert sel.near[0, r, 0]
+        assert np.flatnonzero(sel.near_pairs[0, r, 0]).tolist() == [1]
+    assert not sel.near[0, :4].any()
+    # inside the band the definition still decides by >=: kept iff the ratio >= alpha
+    assert bool(sel.kept[0, 6, 0, 1]) == (eps >= 0)
+
+
+@pytest.mark.parametrize("eps", [5e-3, -5e-3, 5e-4, -5e-4, 1.5e-4, -1.5e-4])
+def test_near_band_silent_outside(eps):
+    """Outside 1e-4 relative the flag stays silent; +-5e-4 relative is only 5e-5 absolute at
+    alpha 0.1, so an absolute band of 1e-4 would fire there."""
+    q, k, v, blk, _ = _band_case(eps)
+    sel = oracle.block_select(q, k, 0, blk, 0.1, scale=1.0)
+    assert not sel.near.any()
+    assert not sel.near_pairs.any()
+    assert bool(sel.kept[0, 6, 0, 1]) == (eps > 0)
+
+
+def test_near_band_scales_with_alpha():
+    """The band is relative to alpha: at alpha 0.5 a pair at 0.5 (1 + 9e-5) is near."""
+    q, k, v, blk, _ = _band_case(9e-5, alpha=0.5)
+    assert oracle.block_select(q, k, 0, blk, 0.5, scale=1.0).near[0, 6, 0]
+    q, k, v, blk, _ = _band_case(2e-4, alpha=0.5)
+    assert not oracle.block_select(q, k, 0, blk, 0.5, scale=1.0).near.any()
+
+
+def _sparse_row_by_hand(q, k, v, p, blk, kept_blocks, scale):
+    """Row p of the block-sparse definition with math.exp loops (q: that row's query): exact
+    keys j <= p of the kept blocks, one pooled term n_b exp(q . kbar_b * scale) vbar_b per
+    skipped earlier block."""
+    ob = p // blk
+    terms = []
+    for j in range(p + 1):
+        if j // blk in kept_blocks:
+            terms.append((sum(q[i] * k[j][i] for i in range(len(q))) * scale, 1.0, list(v[j])))
+    for b in range(ob):
+        if b not in kept_blocks:
+            kb = [sum(k[j][i] for j in range(b * blk, (b + 1) * blk)) / blk for i in range(len(q))]
+            vb = [sum(v[j][i] for j in range(b * blk, (b + 1) * blk)) / blk for i in range(len(q))]
+            terms.append((sum(q[i] * kb[i] for i in range(len(q))) * scale, float(blk), vb))
+    m = max(x for x, _, _ in terms)
+    den = sum(n * math.exp(x - m) for x, n, _ in terms)
+    return [sum(n * math.exp(x - m) * vv[i] for x, n, vv in terms) / den for i in range(len(q))]
+
+
+def test_sparse_for_selection_follows_a_flipped_near_pair():
+    """A selection that decides the near pair the other way gets the definition's output under
+    that selection (checked against a hand-written row); the untouched rows keep the plain
+    result; a selection that differs at a pair outside the band is refused."""
+    q, k, v, blk, _ = _band_case(5e-5, t3=0.0, spread=1.5)
+    base, sel = oracle.sparse(q, k, v, 0, blk, 0.1, scale=1.0)
+    assert sel.kept[0, 6, 0, 1] and sel.kept[0, 7, 0, 1]
+    flipped = sel.kept.copy()
+    flipped[0, 6, 0, 1] = False                      # row 6 pools block 1 instead
+    out, osel, rows = oracle.sparse_for_selection(q, k, v, 0, blk, 0.1, flipped, scale=1.0)
+    assert rows.tolist() == [6]
+    assert osel.near[0, 6, 0]
+    want6 = _sparse_row_by_hand(q[0, 6, 0], k[0, :, 0], v[0, :, 0], 6, blk, {0, 3}, 1.0)
+    want7 = _sparse_row_by_hand(q[0, 7, 0], k[0, :, 0], v[0, :, 0], 7, blk, {0, 1, 3}, 1.0)
+    assert np.max(np.abs(out[0, 6, 0] - want6)) <= 1e-12
+    assert np.max(np.abs(out[0, 7, 0] - want7)) <= 1e-12
+    assert np.max(np.abs(out[0, 7, 0] - base[0, 7, 0])) <= 1e-15
+    # the flip matters: pooling block 1 moves row 6 by several times the parity tolerance
+    assert np.max(np.abs(out[0, 6, 0] - base[0, 6, 0])) > 4 * 5e-3
+    bad = sel.kept.copy()
+    bad[0, 6, 0, 2] = True                           # block 2 is far below the threshold
+    with pytest.raises(ValueError, match="outside the threshold band"):
+        oracle.sparse_for_selection(q, k, v, 0, blk, 0.1, bad, scale=1.0)
