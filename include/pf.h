@@ -246,7 +246,11 @@ pf_status pf_attn_sparse(const pf_shape* shape, const void* q, const void* k, co
  *     rejected with PF_EUNSUPPORTED and a message in pf_last_error().
  *   - Set-up: the first call on each device looks up the buffer's device
  *     address (cudaGetSymbolAddress) with that device current; make that first
- *     call before any stream capture.
+ *     call before any stream capture.  The address is looked up once per device
+ *     for the life of the process and is not looked up again after a
+ *     cudaDeviceReset: do not call this entry point after resetting a device.
+ *   - Shapes: B, Hq, Hkv, d, C below 1 or a negative start_pos are refused
+ *     with PF_EINVAL before the scratch size is considered.
  *   - Sharing: every call uses the same buffer, which keeps the previous call's
  *     contents; nothing in it needs to start at zero (each call writes what it
  *     reads).  Calls that overlap on the GPU (other streams, other host threads)

@@ -63,10 +63,26 @@ extern "C" {
 pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void* k, const void* v,
                                 int32_t start_pos, int32_t block, const pf_sel* sel, void* out,
                                 float* lse, void* stream) {
+  // A shape that pf_attn_sparse would reject as invalid is rejected the same way here, before
+  // its scratch size is computed (a negative or overflowing size must not read as "too big").
+  if (shape == nullptr) {
+    pf::set_error_message("pf_attn_sparse_static: shape is NULL");
+    return PF_EINVAL;
+  }
+  if (shape->B < 1 || shape->Hq < 1 || shape->Hkv < 1 || shape->d < 1 || shape->C < 1 || start_pos < 0) {
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "pf_attn_sparse_static: B, Hq, Hkv, d and C must be >= 1 and start_pos >= 0 (got %d, %d, %d, "
+             "%d, %d, %d)", shape->B, shape->Hq, shape->Hkv, shape->d, shape->C, start_pos);
+    pf::set_error_message(msg);
+    return PF_EINVAL;
+  }
   pf_sparse_sizes z;
   pf_status rc = pf_sparse_query_sizes(shape, start_pos, block, &z);
   if (rc != PF_OK) return rc;
-  if (z.pooled_bytes < 0 || (size_t)z.pooled_bytes > kScratchBytes) {
+  // the same size in floating point: a product past int64 shows up here as too large
+  const double approx = (double)shape->B * shape->Hkv * (double)z.nblk * shape->d * 8.0;
+  if (approx > (double)kScratchBytes * 2.0 || z.pooled_bytes < 0 || (size_t)z.pooled_bytes > kScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
              "pf_attn_sparse_static: this problem needs %lld bytes of scratch but the static buffer "

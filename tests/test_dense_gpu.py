@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import prefill_inputs as pi
-from gpu_util import assert_close, dev, errors, sample_rows, MAX_ABS
+from gpu_util import MAX_ABS, MEAN_ABS, assert_close, dev, errors, sample_rows
 from long_context_prefill_chunked_gb300 import pf
 
 pytestmark = pytest.mark.gpu
@@ -292,11 +292,13 @@ def test_lse_matches_oracle(case):
 
 # --------------------------------------------------------------------------- the bench's launches
 @pytest.mark.slow
-def test_config4_dense_chunked_as_benchmarked():
+def test_config4_dense_chunked_as_benchmarked(tmp_path):
     """The 32K prompt as bench.py runs it: 8 chunks of 4096 causal rows over the previous
     chunks' K/V, chunk outputs written into one [1, 32768, 32, 128] tensor, K/V emitted into a
-    head-major cache, the tail-split workspace on.  Sampled rows of every chunk against the
-    oracle; the cache must be a bit copy."""
+    head-major cache, the tail-split workspace on.  Per chunk 2048 seeded rows, the last 128 rows
+    and every tile-boundary row, all 32 heads, against the oracle (a process pool, one task per
+    chunk and KV head); the cache must be a bit copy."""
+    import oracle_pool
     w = pi.config(4)
     N, CH = w.N, 4096
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
@@ -309,9 +311,13 @@ def test_config4_dense_chunked_as_benchmarked():
                        out=out[:, s:s + CH], out_k=ck[:, :, s:s + CH], out_v=cv[:, :, s:s + CH])
     pfx.stream_status()
     assert torch.equal(ck.transpose(1, 2).contiguous(), K) and torch.equal(cv.transpose(1, 2).contiguous(), V)
-    q64, k64, v64 = w.f64(w.q), w.f64(w.k), w.f64(w.v)
+    root = str(tmp_path)
+    oracle_pool.save_inputs(w, root)
+    tasks = []
     for ci, s in enumerate(range(0, N, CH)):
-        rows = sample_rows(CH, 48, 400 + ci)
-        ref = oracle.dense(q64[:, s:s + CH], k64[:, :s], v64[:, :s], k64[:, s:s + CH], v64[:, s:s + CH], s,
-                           rows=rows)
-        assert_close(out[:, s + rows], ref, "32K chunk at %d" % s)
+        rows = sample_rows(CH, 2048, 400 + ci)
+        oracle_pool.save_result(root, "dense", s, rows, out[0, s + torch.from_numpy(rows).cuda()].cpu().numpy())
+        tasks += [oracle_pool.Task(root, w.dtype, "dense", s, CH, g, w.Hq // w.Hkv) for g in range(w.Hkv)]
+    for (path, s), a in sorted(oracle_pool.summarize(oracle_pool.run_tasks(tasks)).items()):
+        assert a["finite"] and a["n"] >= 2048 * 32 * 128, (s, a)
+        assert a["max"] <= MAX_ABS and a["mean"] <= MEAN_ABS, ("32K chunk at %d" % s, a["max"], a["mean"])

@@ -69,3 +69,19 @@ def test_static_scratch_refuses_oversized_problems(lib):
                                    None)
     assert rc == pf.PF_EUNSUPPORTED
     assert b"static buffer" in lib.pf_last_error()
+
+
+@pytest.mark.parametrize("field,value,start", [("C", 0, 0), ("B", -1, 0), ("Hkv", 0, 0), ("d", -128, 0),
+                                               ("C", 4096, -128)])
+def test_static_scratch_refuses_invalid_shapes(lib, field, value, start):
+    """An invalid shape is PF_EINVAL (as pf_attn_sparse gives), not a scratch-size refusal."""
+    sh = pf.Shape()
+    sh.B, sh.Hq, sh.Hkv, sh.d, sh.C = 1, 8, 2, 128, 4096
+    sh.in_dtype, sh.out_dtype, sh.mask_dtype = pf.PF_BF16, pf.PF_F32, pf.PF_F32
+    setattr(sh, field, value)
+    fake = ctypes.c_void_p(0x100000)
+    sel = pf.Sel(0x100000, 0x100000, 0x100000, 0x100000)
+    rc = lib.pf_attn_sparse_static(ctypes.byref(sh), fake, fake, fake, start, 128, ctypes.byref(sel), fake,
+                                   None, None)
+    assert rc == pf.PF_EINVAL, (rc, lib.pf_last_error())
+    assert b"static buffer" not in lib.pf_last_error()
