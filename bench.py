@@ -6,8 +6,12 @@ bf16, planted block structure) through the whole path:
     previous chunks' K/V, emitting the chunk's K/V into a head-major cache;
   * block-sparse prefill of the same prompt: block index (pool, score,
     select, compact) + exact kept blocks with the pooled correction.
-The metric is dense-equivalent TFLOP/s: 4 * Hq * d * (causal query-key pairs)
-per path, summed, over the step time.
+The metric is dense-equivalent TFLOP/s: 4 * Hq * d * (causal query-key pairs of
+the prompt), counted once per step although both paths compute it, over the
+step time; each path's own TFLOP/s and tokens/s are reported beside it.  The same
+run also measures the 128K-token prompt (32 chunks of 4096 over a growing
+history) through both paths (``long_128k``) and times the oracle in full on
+the three small workloads (``oracle_full``).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -136,27 +140,59 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- oracle legs
 def oracle_sample_rate(w, seconds, seed=0):
-    """Time the float64 oracle on sampled rows of both paths; returns (TFLOP/s equiv, detail)."""
+    """Time the float64 oracle on sampled rows of the last 4096-row chunk, each row through both
+    paths (dense over its 28672-token history + chunk, and block-sparse); a row's dense-equivalent
+    work is counted once.  Returns (TFLOP/s equiv, detail)."""
     import oracle
     g = np.random.default_rng(seed)
     s_last = N_TOK - CHUNK
     q_last = w.f64(w.q[:, s_last:])
     kh, vh = w.f64(w.k[:, :s_last]), w.f64(w.v[:, :s_last])
     kc, vc = w.f64(w.k[:, s_last:]), w.f64(w.v[:, s_last:])
-    q_all, k_all, v_all = w.f64(w.q), w.f64(w.k), w.f64(w.v)
+    k_all, v_all = w.f64(w.k), w.f64(w.v)
     flops = 0.0
     rows_done = 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds:
         rows = np.sort(g.choice(CHUNK, size=16, replace=False))
         oracle.dense(q_last, kh, vh, kc, vc, s_last, rows=rows)
+        oracle.sparse(q_last, k_all, v_all, s_last, BLOCK, ALPHA, rows=rows)
         flops += sum(4.0 * HQ * D * (s_last + r + 1) for r in rows)
-        srows = np.sort(g.choice(N_TOK, size=16, replace=False))
-        oracle.sparse(q_all, k_all, v_all, 0, BLOCK, ALPHA, rows=srows)
-        flops += sum(4.0 * HQ * D * (r + 1) for r in srows)
-        rows_done += 32
+        rows_done += 16
     dt = time.perf_counter() - t0
     return flops / dt / 1e12, {"rows": rows_done, "seconds": dt, "threads": _blas_threads()}
+
+
+def oracle_full_timings():
+    """The oracle timed in full on the three small workloads (every row, every head), and the
+    per-(row, head, key) cost of the largest one extrapolated to the 32K and 128K prompts."""
+    import oracle
+    import prefill_inputs as pi
+    res = {}
+    w1 = pi.config(1)
+    t0 = time.perf_counter()
+    oracle.dense(*(w1.f64(x) for x in w1.chunk_views(0)), 0, mask=pi.causal_mask(256, 0, np.float64))
+    res["config1_s"] = time.perf_counter() - t0
+    w2 = pi.config(2)
+    t0 = time.perf_counter()
+    pairs2 = 0
+    for s in w2.starts:
+        oracle.dense(*(w2.f64(x) for x in w2.chunk_views(s)), s, mask=pi.causal_mask(w2.chunk, s, np.float64))
+        pairs2 += w2.chunk * (s + w2.chunk)
+    res["config2_s"] = time.perf_counter() - t0
+    w3 = pi.config(3)
+    mask, _ = pi.indexer_fold_mask(w3.seed, w3.chunk, 8192)
+    t0 = time.perf_counter()
+    oracle.dense(*(w3.f64(x) for x in w3.chunk_views(8192)), 8192, mask=mask.astype(np.float64))
+    res["config3_s"] = time.perf_counter() - t0
+    per_elem = res["config2_s"] / (pairs2 * w2.Hq)           # seconds per (row, head, key)
+    causal = lambda n, c: sum(c * s + c * (c + 1) // 2 for s in range(0, n, c))
+    res["extrapolated_32k_dense_s"] = per_elem * HQ * causal(N_TOK, CHUNK)
+    res["extrapolated_128k_dense_s"] = per_elem * HQ * causal(131072, CHUNK)
+    res["note"] = ("configs 1-3 timed in full (every row and head, explicit masks); the 32K and 128K "
+                   "figures are EXTRAPOLATED from config 2's cost per (row, head, key), not run")
+    res["cores"] = _blas_threads()
+    return res
 
 
 def _blas_threads():
@@ -211,8 +247,9 @@ def run_reference(args):
         "data": "synthetic (seeded)", "config": {"workload": WORKLOAD % pi.PLANT_BETA},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": per_step[0][1]["threads"],
                          "kind": "oracle", "host": host_cpu(),
-                         "sample": "%d query rows x 32 heads (half from the last dense chunk, half "
-                                   "block-sparse), float64 numpy oracle" % rows},
+                         "sample": "%d query rows x 32 heads of the last 4096-row chunk, each through "
+                                   "the dense and the block-sparse oracle (work counted once), float64 "
+                                   "numpy oracle" % rows},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -264,16 +301,22 @@ def run_case(args):
     K, V = to_dev(w.k), to_dev(w.v)
     Q = to_dev(w.q[:, s:s + CHUNK]) if args.case == "dense-chunk" else to_dev(w.q)
     if args.case == "dense-chunk":
+        # as in the bench step: the chunk's K/V are re-emitted into a head-major cache
         out = torch.empty((1, CHUNK, HQ, D), dtype=torch.float32, device="cuda")
-        run = lambda: pfx.attn_dense(Q, K[:, :s], V[:, :s], K[:, s:s + CHUNK], V[:, s:s + CHUNK], s, out=out)
+        ck = torch.empty((1, HKV, CHUNK, D), dtype=torch.bfloat16, device="cuda")
+        cv = torch.empty_like(ck)
+        run = lambda: pfx.attn_dense(Q, K[:, :s], V[:, :s], K[:, s:s + CHUNK], V[:, s:s + CHUNK], s, out=out,
+                                     out_k=ck, out_v=cv)
         flops = flops_equiv(CHUNK, s)
     else:
         sel = pfx.alloc_selection(Q, K, 0)
         pooled = pfx.alloc_pooled(Q, K, 0)
         out = torch.empty((1, N_TOK, HQ, D), dtype=torch.float32, device="cuda")
+        # sparse-shared: the Metal port's KV-group shared selection (share_group_kernel)
+        rules = pfx.KeepRules(share_kv_group=1) if args.case == "sparse-shared" else None
 
         def run():
-            pfx.block_index(Q, K, 0, BLOCK, ALPHA, sel=sel)
+            pfx.block_index(Q, K, 0, BLOCK, ALPHA, sel=sel, rules=rules)
             pfx.attn_sparse(Q, K, V, 0, sel, pooled=pooled, out=out)
         flops = flops_equiv(N_TOK, 0)
     return _time_case(args, pfx, run, flops, s if args.case == "dense-chunk" else 0)
@@ -298,6 +341,91 @@ def _time_case(args, pfx, run, flops, start):
     return 0
 
 
+# ---------------------------------------------------------------------------- 128K record
+def run_long_128k(pfx, dev, reps=3, warmup=1):
+    """The 128K-token planted prompt (32q/8kv, d128, bf16) as a chunked prefill: 32 chunks of 4096
+    rows over a growing history (0 .. 126,976 rows), each chunk through dense causal prefill
+    (emitting its K/V into a head-major cache, tail-split workspace on) and, separately, through
+    block-sparse prefill (block index + sparse attention with the pooled correction, block 128,
+    alpha 0.1; one pooled-key buffer and workspace for the prompt, each chunk pooling only its
+    own blocks).  CUDA events per call on the launching stream; the median over `reps` passes
+    (inputs are 1.5 GB, far beyond L2).  Skip share is weighted by dense work: per (head, query
+    tile) the dense path runs its off-diagonal key tiles plus half a diagonal tile, the sparse
+    path its kept off-diagonal tiles plus the same half (pooled tiles not counted)."""
+    import torch
+    import prefill_inputs as pi
+    w = pi.config(5)
+    N, C = w.N, w.chunk
+    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    Q, K, V = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    starts = w.starts
+    out = torch.empty((1, C, HQ, D), dtype=torch.float32, device=dev)
+    cache_k = torch.empty((1, HKV, N, D), dtype=torch.bfloat16, device=dev)
+    cache_v = torch.empty_like(cache_k)
+    # one pooled-key buffer and one sparse workspace for the whole prompt: each chunk pools only
+    # its own blocks (the history's block means do not change)
+    kbar = pfx.alloc_kbar(Q[:, :C], K, N, BLOCK)
+    pooled = pfx.alloc_pooled(Q[:, :C], K, 0, BLOCK, max_keys=N)
+    sels = [pfx.alloc_selection(Q[:, s:s + C], K[:, :s + C], s, BLOCK, kbar=kbar, pooled_blocks=s // BLOCK)
+            for s in starts]
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    dense_t, index_t, attn_t = [], [], []
+    for it in range(warmup + reps):
+        e = {"d": [(ev(), ev()) for _ in starts], "i": [(ev(), ev()) for _ in starts],
+             "a": [(ev(), ev()) for _ in starts]}
+        for i, s in enumerate(starts):
+            e["d"][i][0].record(stream)
+            pfx.attn_dense(Q[:, s:s + C], K[:, :s], V[:, :s], K[:, s:s + C], V[:, s:s + C], s, out=out,
+                           out_k=cache_k[:, :, s:s + C], out_v=cache_v[:, :, s:s + C], stream=stream)
+            e["d"][i][1].record(stream)
+        for i, s in enumerate(starts):
+            q = Q[:, s:s + C]
+            e["i"][i][0].record(stream)
+            pfx.block_index(q, K[:, :s + C], s, BLOCK, ALPHA, sel=sels[i], stream=stream)
+            e["i"][i][1].record(stream)
+            e["a"][i][0].record(stream)
+            pfx.attn_sparse(q, K[:, :s + C], V[:, :s + C], s, sels[i], block=BLOCK, pooled=pooled, out=out,
+                            stream=stream)
+            e["a"][i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        if it >= warmup:
+            dense_t.append([a.elapsed_time(b) for a, b in e["d"]])
+            index_t.append([a.elapsed_time(b) for a, b in e["i"]])
+            attn_t.append([a.elapsed_time(b) for a, b in e["a"]])
+    pfx.stream_status(stream)
+    med = lambda runs: statistics.median(sum(r) for r in runs)
+    t_dense, t_index, t_attn = med(dense_t), med(index_t), med(attn_t)
+    t_sparse = t_index + t_attn
+    dense_w = sparse_w = 0.0
+    for s, sel in zip(starts, sels):
+        tc = sel.tile_cnt.cpu().numpy().astype(np.float64)             # [1, Hq, nqt]
+        ob = s // BLOCK + np.arange(tc.shape[-1])
+        dense_w += HQ * (ob + 0.5).sum()
+        sparse_w += (tc - 1 + 0.5).sum()
+    skip = 1.0 - sparse_w / dense_w
+    flops = sum(flops_equiv(C, s) for s in starts)
+    del Q, K, V, cache_k, cache_v, sels, kbar, pooled, out
+    torch.cuda.empty_cache()
+    return {
+        "workload": "128K-token prompt, 32q/8kv, d128, bf16, planted blocks (beta %g), 32 chunks x 4096 "
+                    "over a growing history; block 128, alpha 0.1" % w.beta,
+        "dense_ms": t_dense, "dense_tflops": flops / (t_dense * 1e-3) / 1e12,
+        "dense_tokens_per_s": N / (t_dense * 1e-3),
+        "sparse_ms": t_sparse, "sparse_index_ms": t_index, "sparse_attn_ms": t_attn,
+        "sparse_tflops_equiv": flops / (t_sparse * 1e-3) / 1e12, "sparse_tokens_per_s": N / (t_sparse * 1e-3),
+        "skip_share_flop_weighted": skip,
+        "speedup": t_dense / t_sparse,
+        "efficiency": (t_dense / t_sparse) * (1.0 - skip),
+        "efficiency_note": "(t_dense / t_sparse) * (1 - skip); 1 = sparse time exactly in proportion to "
+                           "the dense work it keeps",
+        "dense_ms_per_chunk": [statistics.median(r[i] for r in dense_t) for i in range(len(starts))],
+        "sparse_ms_per_chunk": [statistics.median(a[i] + b[i] for a, b in zip(index_t, attn_t))
+                                for i in range(len(starts))],
+        "reps": reps,
+    }
+
+
 # ---------------------------------------------------------------------------- ours
 def main():
     ap = argparse.ArgumentParser()
@@ -308,11 +436,14 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse", "sparse-128k-chunk",
-                                                       "indexed-config3", "mask-config3"],
+    ap.add_argument("--no-long", action="store_true", help="skip the 128K-token record")
+    ap.add_argument("--long-reps", type=int, default=3)
+    ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse", "sparse-shared",
+                                                       "sparse-128k-chunk", "indexed-config3", "mask-config3"],
                     help="profiling cases, timings only: dense-chunk (one 4096-row chunk at "
-                         "--start), sparse (the 32K block-sparse pair), sparse-128k-chunk (the "
-                         "pair for the last 4096-row chunk of the 128K prompt), indexed-config3 / "
+                         "--start, K/V re-emitted into a cache), sparse (the 32K block-sparse pair), "
+                         "sparse-shared (the same with KV-group shared selection), sparse-128k-chunk "
+                         "(the pair for the last 4096-row chunk of the 128K prompt), indexed-config3 / "
                          "mask-config3 (config 3's selection as keep lists / as a folded mask)")
     ap.add_argument("--start", type=int, default=N_TOK - CHUNK,
                     help="dense-chunk case: the chunk's first token (a multiple of 4096)")
@@ -408,8 +539,11 @@ def main():
 
     f_dense = sum(flops_equiv(CHUNK, s) for s in starts)
     f_sparse = flops_equiv(N_TOK, 0)
-    value = weak_scaling_value(f_dense + f_sparse, ms_step, world)
-    tokens_per_s = world * 2 * N_TOK / (ms_step * 1e-3)
+    # the step computes the prompt's causal attention twice (dense, then block-sparse): its
+    # dense-equivalent work and its tokens are counted once
+    f_prompt = f_dense
+    value = weak_scaling_value(f_prompt, ms_step, world)
+    tokens_per_s = world * N_TOK / (ms_step * 1e-3)
 
     # dominant kernel: the dense attention launches (8 per step)
     d_ms = sum(map(sum, dense_ms)) / args.steps
@@ -495,6 +629,13 @@ def main():
                    "l2": "flushed between steps (256 MB write outside the step window)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": tokens_per_s,
+        "step_note": "one step = the 32K prompt through dense chunked prefill (8 x 4096) and through "
+                     "block-sparse prefill; value and tokens_per_s count the prompt once per step; "
+                     "each path's own rate is below",
+        "dense_chunked_tflops": f_dense / (d_ms * 1e-3) / 1e12,
+        "dense_chunked_tokens_per_s": N_TOK / (d_ms * 1e-3),
+        "block_sparse_tflops_equiv": f_sparse / ((statistics.mean(index_ms) + statistics.mean(sparse_ms)) * 1e-3) / 1e12,
+        "block_sparse_tokens_per_s": N_TOK / ((statistics.mean(index_ms) + statistics.mean(sparse_ms)) * 1e-3),
         "paths": {
             "dense_chunked": {"ms": sum(map(sum, dense_ms)) / args.steps,
                               "tflops_equiv": f_dense / (d_ms * 1e-3) / 1e12,
@@ -510,20 +651,24 @@ def main():
                      "kernel": "attn_fwd_kernel<causal> (8 launches per step; window includes the "
                                "chunk's two cache-layout copies)",
                      "peak_source": "%s bf16_tflops (burst)" % peak_src},
-        "e2e": {"value": weak_scaling_value(f_dense + f_sparse, e2e_ms, world), "unit": "TFLOP/s",
+        "e2e": {"value": weak_scaling_value(f_prompt, e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelining": "two buffer sets; step i+1's H2D and step i-1's D2H overlap step i on "
                               "their own streams; window from the first H2D to the last D2H"},
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if world == 1 and not args.no_long:
+        line["long_128k"] = run_long_128k(pfx, dev, reps=args.long_reps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, det = oracle_sample_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": det["threads"], "kind": "oracle",
                                 "host": host_cpu(),
-                                "sample": "%d query rows x 32 heads in %.1f s: half from the last dense "
-                                          "chunk (keys 28672..32767), half block-sparse; float64 numpy "
-                                          "oracle" % (det["rows"], det["seconds"])}
+                                "sample": "%d query rows x 32 heads of the last 4096-row chunk (keys "
+                                          "28672..32767) in %.1f s, each row through the dense and the "
+                                          "block-sparse oracle (work counted once); float64 numpy oracle"
+                                          % (det["rows"], det["seconds"])}
+        line["oracle_full"] = oracle_full_timings()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

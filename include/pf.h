@@ -72,7 +72,7 @@ typedef struct {
   int32_t B;            /* batch */
   int32_t Hq;           /* query heads */
   int32_t Hkv;          /* KV heads; Hq % Hkv == 0 */
-  int32_t d;            /* head dim: 64 or 128 */
+  int32_t d;            /* head dim: 64, 128 or 256 */
   int32_t C;            /* query rows in this call (the chunk), >= 1 */
   pf_dtype in_dtype;    /* q/k/v element type: PF_F16 or PF_BF16 */
   pf_dtype out_dtype;   /* out element type: PF_F32, PF_BF16 or PF_F16 */
@@ -162,18 +162,33 @@ pf_status pf_attn_indexed(const pf_shape* shape, const void* q, const void* k_hi
 pf_status pf_indexed_workspace_bytes(const pf_shape* shape, int32_t start_pos, int64_t* bytes);
 
 /* Block selection produced by pf_block_index and consumed by pf_attn_sparse.
- * nblk = ceil((start_pos + C) / block); nqt = ceil(C / 128); W = ceil(nblk / 32). */
+ * nblk = ceil((start_pos + C) / block); nqt = ceil(C / 128); W = ceil(nblk / 32);
+ * cap = capacity, or nblk when capacity is 0.
+ *
+ * Chunked prefill: the pooled keys and values of the history's blocks do not change from one
+ * chunk to the next, so a prompt processed in chunks can keep ONE kbar buffer (and one
+ * pf_attn_sparse workspace) for all its chunks, sized for its last chunk (capacity = that
+ * chunk's nblk), and pass pooled_blocks = the blocks an earlier call of the same prompt has
+ * already pooled into them: only blocks pooled_blocks .. nblk - 1 are pooled again. */
 typedef struct {
   uint32_t* row_bits;  /* [B, Hq, C, W]: bit (b % 32) of word b / 32 set iff the row keeps block b */
   int32_t* tile_list;  /* [B, Hq, nqt, nblk]: ascending union of the kept blocks of the tile's rows */
   int32_t* tile_cnt;   /* [B, Hq, nqt]: valid entries of tile_list */
-  float* kbar;         /* 2 * B*Hkv*nblk*d floats: the fp32 pooled (mean) keys [B, Hkv, nblk, d],
+  float* kbar;         /* 2 * B*Hkv*cap*d floats: the fp32 pooled (mean) keys [B, Hkv, cap, d],
                           then the library's 16-bit split of them (hi = round(mean), lo =
-                          round(mean - hi), each [B, Hkv, nblk, d] in the q/k type) */
+                          round(mean - hi), each [B, Hkv, cap, d] in the q/k type); blocks
+                          nblk .. cap - 1 are not touched */
+  int32_t capacity;    /* key blocks per (batch, KV head) in kbar and in pf_attn_sparse's
+                          workspace; 0 means nblk; otherwise >= nblk (PF_EINVAL) */
+  int32_t pooled_blocks; /* leading blocks whose means kbar (pf_block_index) or the workspace
+                          (pf_attn_sparse) already holds from an earlier call on the same keys
+                          and values with the same capacity; 0 pools every block; at most
+                          start_pos / block (only whole history blocks; PF_EINVAL otherwise) */
 } pf_sel;
 
 /* Element counts of the pf_sel buffers (kbar_elems counts floats) and the byte size of
- * the pf_attn_sparse workspace. */
+ * the pf_attn_sparse workspace, for capacity = nblk.  For buffers shared by the chunks of
+ * one prompt, query the last chunk: its kbar_elems and pooled_bytes cover every chunk. */
 typedef struct {
   int64_t nblk, nqt, words;
   int64_t row_bits_elems, tile_list_elems, tile_cnt_elems, kbar_elems;
@@ -218,9 +233,10 @@ pf_status pf_block_index(const pf_shape* shape, const void* q, const void* k, in
  * head h, kept set K_i from sel (row_bits), skipped set R_i = {b < ob} \ K_i:
  *   out = (sum_{j <= p, j/block in K_i} e^(l_j - m) v_j + sum_{b in R_i} n_b e^(s_ib - m) vbar_b)
  *       / (sum_{j <= p, j/block in K_i} e^(l_j - m)     + sum_{b in R_i} n_b e^(s_ib - m)).
- * pooled: caller-allocated workspace of pf_sparse_sizes.pooled_bytes; on
- * return it starts with vbar, the fp32 block means of v, [B, Hkv, nblk, d];
- * the rest is scratch.  sel must come from pf_block_index on the same q, k,
+ * pooled: caller-allocated workspace of pf_sparse_sizes.pooled_bytes (for
+ * sel->capacity blocks); on return it starts with vbar, the fp32 block means of
+ * v, [B, Hkv, cap, d]; the rest is scratch, except that with sel->pooled_blocks
+ * > 0 it must still hold what the earlier call of the same prompt left there.  sel must come from pf_block_index on the same q, k,
  * start_pos and block.  lse (optional, [B, Hq, C] fp32): the log of the
  * denominator above, exact and pooled terms, as for pf_attn_dense.
  */
@@ -255,7 +271,9 @@ pf_status pf_attn_sparse(const pf_shape* shape, const void* q, const void* k, co
  *     contents; nothing in it needs to start at zero (each call writes what it
  *     reads).  Calls that overlap on the GPU (other streams, other host threads)
  *     race on the buffer: order them.
- *   - The pooled block means stay internal (no vbar output).
+ *   - The pooled block means stay internal (no vbar output).  sel->pooled_blocks
+ *     must be 0 (PF_EUNSUPPORTED otherwise): the shared buffer cannot carry one
+ *     prompt's pooled blocks from call to call.
  */
 #define PF_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -126,11 +126,35 @@ struct BlockWalk {
   }
 };
 
-__device__ __forceinline__ void ld_row128(uint32_t taddr, float (&x)[128]) {
-  uint32_t r[128];
-  tmem_ld128_wait(taddr, r);
+// Key tiles in order from a bitmap of 128-key blocks: each set bit gives `tpb` consecutive
+// tiles of 128 / tpb keys (tpb = 1 or 2).
+template <int TPB>
+struct TileWalk {
+  BlockWalk walk;
+  int cur, half;
+  // starts at the j0-th tile of the walk
+  __device__ void init(const uint32_t* bitmap, int j0) {
+    walk.init(bitmap);
+    walk.skip(j0 / TPB);
+    half = j0 % TPB;
+    cur = half ? walk.next() : 0;
+  }
+  __device__ int next() {
+    if (half == 0) cur = walk.next();
+    const int kt = cur * TPB + half;
+    half = (half + 1 == TPB) ? 0 : half + 1;
+    return kt;
+  }
+};
+
+// One row's scores of a key tile from tensor memory (KT = 128 or 64 columns).
+template <int KT>
+__device__ __forceinline__ void ld_row(uint32_t taddr, float (&x)[KT]) {
+  uint32_t r[KT];
+  if constexpr (KT == 128) tmem_ld128_wait(taddr, r);
+  else tmem_ld64_wait(taddr, r);
 #pragma unroll
-  for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < KT; ++i) x[i] = __uint_as_float(r[i]);
 }
 
 // 32 consecutive output values of one row, already divided by l, in the output type.
@@ -153,9 +177,17 @@ __device__ __forceinline__ void store_out32(const AttnArgs& a, long long off, co
   }
 }
 
-template <int MODE>
+// WIDE: head_dim 256.  Key tiles are 64 keys (a 128-key block is two tiles), pooled tiles 64
+// pooled blocks, one query head per CTA; the Q tile (64 KB) and the K / V rings keep their sizes,
+// and O (256 fp32 columns) sits at tensor-memory column 256.
+template <int MODE, bool WIDE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnArgs a) {
+  constexpr int KT = WIDE ? 64 : 128;          // keys per key tile (S columns)
+  constexpr int TPB = kTile / KT;              // key tiles per 128-key block
+  constexpr int PT = WIDE ? 64 : 128;          // pooled blocks per pooled tile
+  constexpr uint32_t O_COL = WIDE ? 256u : 128u;  // O's first column in the slot's tensor memory
+  constexpr uint32_t KBOX = KT * 128u;         // bytes of one 64-column box of a K / V tile
   // a packed explicit mask is launched as bits, then as values: the launch that does not match
   // the packing pass's verdict returns before it touches anything (the whole CTA alike)
   if (MODE == MODE_MASKB && __ldg(a.mask_nonbinary) != 0) return;
@@ -288,15 +320,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   int n_pool = 0, n_tiles;
   if (MODE == MODE_CAUSAL) {
-    n_tiles = ob + 1;
+    n_tiles = (ob + 1) * TPB;
   } else if (MODE == MODE_MASK) {
-    n_tiles = (a.T + kTile - 1) / kTile;
+    n_tiles = (a.T + KT - 1) / KT;
   } else if (MODE == MODE_MASKB) {
-    n_tiles = *n_ex_slot >= 0 ? *n_ex_slot : (a.T + kTile - 1) / kTile;
+    n_tiles = *n_ex_slot >= 0 ? *n_ex_slot * TPB : (a.T + KT - 1) / KT;
   } else {
-    n_pool = (ob + kTile - 1) / kTile;
-    n_tiles = n_pool + *n_ex_slot;
+    n_pool = (ob + PT - 1) / PT;
+    n_tiles = n_pool + *n_ex_slot * TPB;
   }
+  const int n_total = n_tiles;  // the unit's key tiles (a split part runs a range of them)
   // a split unit's part covers key tiles [j0, j0 + n_tiles); loops below count locally from 0
   int j0 = 0;
   const bool has_last_tile = split < 0 || part == a.split_k - 1;
@@ -313,11 +346,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const int nd = a.d / 64;
-      const uint32_t tile_bytes = (uint32_t)nd * 16384u;
+      const uint32_t tile_bytes = (uint32_t)nd * KBOX;  // one K or V tile: nd boxes of KT rows
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.kh);
       tma_prefetch_desc(&maps.vh);
-      mbar_arrive_expect_tx(BAR(B_Q), tile_bytes * (uint32_t)a.slots);
+      mbar_arrive_expect_tx(BAR(B_Q), (uint32_t)nd * 16384u * (uint32_t)a.slots);
       for (int sl = 0; sl < a.slots; ++sl)
         for (int c = 0; c < nd; ++c)
           tma_load_4d(sb + SM_Q + 32768u * sl + 16384u * c, &maps.q, BAR(B_Q), 64 * c, h0 + sl,
@@ -327,9 +360,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int st = 0; st < NSV; ++st) last_v[st] = -1;
       // key tiles come from the kept-block bitmap (sparse, binary masks) or in order
       const bool walked = MODE == MODE_SPARSE || (MODE == MODE_MASKB && *n_ex_slot >= 0);
-      BlockWalk walk;
-      if (walked) walk.init(kept_bm);
-      if (MODE == MODE_MASKB && walked && n_tiles > 0) walk.skip(j0);  // sparse units never split
+      TileWalk<TPB> walk;
+      if (walked) walk.init(kept_bm, MODE == MODE_MASKB ? j0 : 0);  // sparse units never split
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NSK, use = j / NSK;
         const int sv = j % NSV, usev = j / NSV;
@@ -338,18 +370,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (MODE == MODE_SPARSE && j < n_pool) {
           mk = &maps.kbar;  // pooled keys [B, Hkv, nblk, d]: rows = pooled blocks
           mv = &maps.vbar;
-          c1 = j * kTile;
+          c1 = j * PT;
           c2 = g;
         } else {
           const int kt = walked ? walk.next() : j0 + j;
           if (kt < a.n_hist_tiles) {
             mk = &maps.kh;
             mv = &maps.vh;
-            c2 = kt * kTile;
+            c2 = kt * KT;
           } else {
             mk = &maps.kc;
             mv = &maps.vc;
-            c2 = kt * kTile - a.s;
+            c2 = kt * KT - a.s;
           }
           c1 = g;
         }
@@ -358,14 +390,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         mbar_arrive_expect_tx(BAR(B_KF + st), tile_bytes);
         for (int c = 0; c < nd; ++c)
-          tma_load_4d(sb + SM_K + 32768u * st + 16384u * c, mk, BAR(B_KF + st), 64 * c, c1, c2, b);
+          tma_load_4d(sb + SM_K + 32768u * st + KBOX * c, mk, BAR(B_KF + st), 64 * c, c1, c2, b);
         last_k[st] = use;
         if (usev > 0 && !mbar_wait(BAR(B_VE + sv), (usev - 1) & 1, a.timeout, abort_flag, a.status,
                                    (R_PROD << 8) | (B_VE + sv)))
           break;
         mbar_arrive_expect_tx(BAR(B_VF + sv), tile_bytes);
         for (int c = 0; c < nd; ++c)
-          tma_load_4d(sb + SM_V + 32768u * sv + 16384u * c, mv, BAR(B_VF + sv), 64 * c, c1, c2, b);
+          tma_load_4d(sb + SM_V + 32768u * sv + KBOX * c, mv, BAR(B_VF + sv), 64 * c, c1, c2, b);
         last_v[sv] = usev;
       }
       if (*abort_flag) {  // let this warp's copies land before the CTA exits
@@ -380,30 +412,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = make_idesc_f16((uint32_t)a.ab_type, 128, 128, 0);
+      const uint32_t idesc_qk = make_idesc_f16((uint32_t)a.ab_type, 128, KT, 0);
       const uint32_t idesc_pv = make_idesc_f16(0u, 128, (uint32_t)a.d, 1);  // fp16 P x fp16 V
       const int kq = a.d / 16;
-      // descriptors are built once; a k-step only advances the start-address field
+      // descriptors are built once; a k-step only advances the start-address field.  Q boxes
+      // (128 rows x 64 columns) are 16 KB apart, K / V boxes (KT rows) KBOX apart.
       const uint64_t dq0 = make_sdesc_sw128(sb + SM_Q, 16, 1024);
       const uint64_t dk0 = make_sdesc_sw128(sb + SM_K, 16, 1024);
-      const uint64_t dv0 = make_sdesc_sw128(sb + SM_V, 16384, 1024);
+      const uint64_t dv0 = make_sdesc_sw128(sb + SM_V, KBOX, 1024);
       auto issue_qk = [&](int sl, int st) {
         const uint32_t d_tmem = tmem + 256u * sl;
         const uint64_t aq = dq0 + ((32768u * sl) >> 4);
         const uint64_t bk = dk0 + ((32768u * st) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
           if (kk < kq) {
-            const uint32_t off = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-            mma_ss(d_tmem, aq + off, bk + off, idesc_qk, kk > 0 ? 1u : 0u);
+            const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+            const uint32_t offb = (KBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
+            mma_ss(d_tmem, aq + offa, bk + offb, idesc_qk, kk > 0 ? 1u : 0u);
           }
         }
       };
       auto issue_pv = [&](int sl, int st, bool acc) {
-        const uint32_t d_tmem = tmem + 256u * sl + 128u;
+        const uint32_t d_tmem = tmem + 256u * sl + O_COL;
         const uint64_t bv = dv0 + ((32768u * st) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
+        for (int kk = 0; kk < KT / 16; ++kk)
           mma_ts(d_tmem, tmem + 256u * sl + 8u * kk, bv + ((2048u * kk) >> 4), idesc_pv,
                  (acc || kk > 0) ? 1u : 0u);
       };
@@ -459,7 +493,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp >= 10 && a.convert_v) {
     // ------------------------------------------------------------ V converters
     const int ct = threadIdx.x - 320;  // 0 .. 32*kConvWarps-1
-    const int nvec = (a.d / 64) * 1024;  // 16-byte vectors per V tile
+    const int nvec = KT * a.d / 8;       // 16-byte vectors per V tile
     float vmax = 0.f;                    // largest |v| seen (bf16 values are exact in fp32)
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % NSV;
@@ -495,7 +529,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t t_s = tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl;
-    const uint32_t t_o = t_s + 128u;
+    const uint32_t t_o = t_s + O_COL;
     const int h = h0 + sl;
     const int row = q0 + r;
     const bool valid = row < a.C;
@@ -504,42 +538,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bits_row = a.row_bits + ((long long)(b * a.Hq + h) * a.C + row) * a.words;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    // MODE_MASKB: one 16-byte word group of mask bits per row and key tile, loaded before the
-    // step's score wait (padding rows read none and mask nothing).  Loading a step ahead
-    // instead holds four more registers across the loop and spills: slower.
-    const uint4* mbits = nullptr;
-    if (MODE == MODE_MASKB && valid)
-      mbits = reinterpret_cast<const uint4*>(a.mask_bits + (long long)row * a.mask_words);
+    // MODE_MASKB: one 16-byte (8-byte for 64-key tiles) word group of mask bits per row and
+    // key tile, loaded before the step's score wait (padding rows read none and mask nothing).
+    // Loading a step ahead instead holds four more registers across the loop and spills: slower.
+    const uint32_t* mbits = nullptr;
+    if (MODE == MODE_MASKB && valid) mbits = a.mask_bits + (long long)row * a.mask_words;
     const bool mwalk = MODE == MODE_MASKB && *n_ex_slot >= 0;
-    BlockWalk walk;
-    if (MODE == MODE_SPARSE || mwalk) walk.init(kept_bm);
-    if (mwalk && n_tiles > 0) walk.skip(j0);
+    TileWalk<TPB> walk;
+    if (MODE == MODE_SPARSE || mwalk) walk.init(kept_bm, mwalk ? j0 : 0);
     for (int j = 0; j < n_tiles; ++j) {
-      uint4 bw = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+      uint32_t wq[KT / 32];
+#pragma unroll
+      for (int q = 0; q < KT / 32; ++q) wq[q] = 0xffffffffu;
       if (MODE == MODE_MASKB) {
         const int kt = mwalk ? walk.next() : j0 + j;
-        if (mbits != nullptr) bw = __ldg(mbits + kt);
+        if (mbits != nullptr) {
+          if constexpr (KT == 128) {
+            const uint4 bw = __ldg(reinterpret_cast<const uint4*>(mbits) + kt);
+            wq[0] = bw.x;
+            wq[1] = bw.y;
+            wq[2] = bw.z;
+            wq[3] = bw.w;
+          } else {
+            const uint2 bw = __ldg(reinterpret_cast<const uint2*>(mbits) + kt);
+            wq[0] = bw.x;
+            wq[1] = bw.y;
+          }
+        }
       }
       ok = wait_all(BAR(B_SF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
                     (R_SOFT << 8) | (B_SF + sl));
       if (!ok) break;
       tc_fence_after();
-      float x[128];
-      ld_row128(t_s, x);
+      float x[KT];
+      ld_row<KT>(t_s, x);
       float xs = a.scale_log2, bias = 0.f;
       bool row_skip = false;  // sparse: this row did not keep the tile's block
       if (MODE == MODE_CAUSAL) {
-        if (j == n_tiles - 1 && has_last_tile) {  // diagonal tile: key q0 + c visible iff c <= r
+        // the diagonal block's tiles (its last TPB): key q0 + off + c is visible iff off + c <= r
+        const int gt = j0 + j;
+        if (has_last_tile && gt >= n_total - TPB) {
+          const int off = (gt - (n_total - TPB)) * KT;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > r) x[c] = -INFINITY;
+          for (int c = 0; c < KT; ++c)
+            if (c + off > r) x[c] = -INFINITY;
         }
       } else if (MODE == MODE_MASKB) {
         // bit set = kept (value 0); dropped keys (and keys past T, whose bits are 0) are -inf;
         // a word of 32 kept keys (most words of a causal-like mask) needs no selects
-        const uint32_t wq[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < KT / 32; ++q)
           if (wq[q] != 0xffffffffu) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -547,13 +595,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
       } else if (MODE == MODE_MASK) {
         xs = 1.f;
-        const int key0 = (j0 + j) * kTile;
-        if (valid && a.mask_vec && key0 + kTile <= a.T) {
+        const int key0 = (j0 + j) * KT;
+        if (valid && a.mask_vec && key0 + KT <= a.T) {
           if (a.mask_f16) {
             const uint4* mp = reinterpret_cast<const uint4*>(
                 reinterpret_cast<const __half*>(a.mask) + (long long)row * a.mask_ld + key0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 32 columns at a time keeps the loads in registers
+            for (int q = 0; q < KT / 32; ++q) {  // 32 columns at a time keeps the loads in registers
               uint4 w4[4];
 #pragma unroll
               for (int v = 0; v < 4; ++v) w4[v] = __ldg(mp + 4 * q + v);
@@ -574,7 +622,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float4* mp = reinterpret_cast<const float4*>(
                 reinterpret_cast<const float*>(a.mask) + (long long)row * a.mask_ld + key0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < KT / 32; ++q) {
               float4 w4[8];
 #pragma unroll
               for (int v = 0; v < 8; ++v) w4[v] = __ldg(mp + 8 * q + v);
@@ -591,7 +639,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         } else {  // ragged last tile, unaligned rows or a padding row: element loads
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < KT / 32; ++q) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int c = 32 * q + i;
@@ -609,12 +657,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       } else {  // MODE_SPARSE
         if (j < n_pool) {
-          // pooled keys: column c is block j*128 + c; a row takes it iff the
+          // pooled keys: column c is block j*PT + c; a row takes it iff the
           // block is an earlier candidate (< ob) that the row did not keep
           bias = a.log2_nb;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int wi = j * 4 + q;
+          for (int q = 0; q < PT / 32; ++q) {
+            const int wi = j * (PT / 32) + q;
             const uint32_t w = (bits_row != nullptr && wi < a.words) ? __ldg(bits_row + wi) : 0u;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -623,11 +671,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
         } else {
-          const int kb = walk.next();
-          if (kb == ob) {
+          const int kt = walk.next();
+          const int kb = kt / TPB;
+          if (kb == ob) {  // the diagonal block: key q0 + off + c is visible iff off + c <= r
+            const int off = (kt % TPB) * KT;
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c > r) x[c] = -INFINITY;
+            for (int c = 0; c < KT; ++c)
+              if (c + off > r) x[c] = -INFINITY;
           } else {
             // a row that did not keep the block gets P = 0 and leaves its max alone
             // (row max and offset -inf below) instead of masking 128 scores
@@ -638,7 +688,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // ---- online softmax (log2 domain)
       float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
+      for (int c = 4; c < KT; c += 4) {
         mx0 = fmaxf(mx0, x[c]);
         mx1 = fmaxf(mx1, x[c + 1]);
         mx2 = fmaxf(mx2, x[c + 2]);
@@ -666,7 +716,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float off = row_skip ? -INFINITY : bias - ((m == -INFINITY) ? 0.f : m);
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < KT / 32; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -872,15 +922,15 @@ __global__ void kv_relayout_kernel(const uint16_t* __restrict__ src, uint16_t* _
   }
 }
 
-template <int MODE>
+template <int MODE, bool WIDE>
 cudaError_t launch_mode(const AttnMaps& maps, const AttnArgs& a, cudaStream_t st) {
   static std::atomic<int> configured[64];
-  cudaError_t e =
-      ensure_dynamic_smem(reinterpret_cast<const void*>(attn_fwd_kernel<MODE>), SM_ALLOC, configured);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(attn_fwd_kernel<MODE, WIDE>), SM_ALLOC,
+                                      configured);
   if (e != cudaSuccess) return e;
   const int units = a.n_qt * a.n_hp * a.B;
   const int grid = a.n_whole + (units - a.n_whole) * a.split_k;
-  attn_fwd_kernel<MODE><<<grid, kAttnThreads, SM_ALLOC, st>>>(maps, a);
+  attn_fwd_kernel<MODE, WIDE><<<grid, kAttnThreads, SM_ALLOC, st>>>(maps, a);
   ++t_launches;
   return cudaGetLastError();
 }
@@ -888,11 +938,19 @@ cudaError_t launch_mode(const AttnMaps& maps, const AttnArgs& a, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaStream_t st) {
+  if (a.d == 256) {
+    switch (mode) {
+      case MODE_CAUSAL: return launch_mode<MODE_CAUSAL, true>(maps, a, st);
+      case MODE_MASK: return launch_mode<MODE_MASK, true>(maps, a, st);
+      case MODE_MASKB: return launch_mode<MODE_MASKB, true>(maps, a, st);
+      default: return launch_mode<MODE_SPARSE, true>(maps, a, st);
+    }
+  }
   switch (mode) {
-    case MODE_CAUSAL: return launch_mode<MODE_CAUSAL>(maps, a, st);
-    case MODE_MASK: return launch_mode<MODE_MASK>(maps, a, st);
-    case MODE_MASKB: return launch_mode<MODE_MASKB>(maps, a, st);
-    default: return launch_mode<MODE_SPARSE>(maps, a, st);
+    case MODE_CAUSAL: return launch_mode<MODE_CAUSAL, false>(maps, a, st);
+    case MODE_MASK: return launch_mode<MODE_MASK, false>(maps, a, st);
+    case MODE_MASKB: return launch_mode<MODE_MASKB, false>(maps, a, st);
+    default: return launch_mode<MODE_SPARSE, false>(maps, a, st);
   }
 }
 

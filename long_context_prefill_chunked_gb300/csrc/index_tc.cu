@@ -12,8 +12,8 @@
 // are computed to about 2^-17 relative error: kbar (fp32 block means) is split
 // into kbar_hi = bf16(kbar) and kbar_lo = bf16(kbar - kbar_hi) and each score is
 // accumulated in fp32 tensor memory as q . kbar_hi + q . kbar_lo (q is bf16 and
-// exact).  Pass 1 streams every pooled tile (128 blocks) once to find the row
-// maximum, pass 2 streams them again and thresholds.
+// exact).  Pass 1 streams every pooled tile (128 blocks; 64 at head dim 256) once
+// to find the row maximum, pass 2 streams them again and thresholds.
 //
 // One CTA = (batch, 128-row query tile, `slots` query heads of one KV group):
 //   warps 0-3 / 4-7  row threads of slot 0 / 1 (thread t owns row t = TMEM lane t)
@@ -74,8 +74,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
   }
 }
 
+// WIDE: head dim 256 -- pooled tiles of 64 blocks (hi and lo tiles keep the 32 KB size), one
+// query head per CTA (its 64 KB query tile fills both slots' room).
+template <bool WIDE>
 __global__ void __launch_bounds__(kIndexThreads, 1)
     index_tc_kernel(const __grid_constant__ IndexMaps maps, const IndexArgs a) {
+  constexpr int PT = WIDE ? 64 : 128;     // pooled blocks per pooled tile (score columns)
+  constexpr uint32_t PBOX = PT * 128u;    // bytes of one 64-column box of a pooled tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -95,7 +100,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   const int g = h0 / a.G;
   const int q0 = qt * kTile;
   const int ob = (a.s + q0) / kTile;           // diagonal block; candidates 0 .. ob-1
-  const int np = (ob + kTile - 1) / kTile;     // pooled tiles holding the candidates
+  const int np = (ob + PT - 1) / PT;           // pooled tiles holding the candidates
   const int nsteps = 2 * np;                   // pass 1 and pass 2
 
   if (threadIdx.x == 0) {
@@ -126,7 +131,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     // ---------------------------------------------------------------- producer
     if (lane == 0 && nsteps > 0) {
       const int nd = a.d / 64;
-      const uint32_t box = 16384u;
+      const uint32_t box = 16384u;  // a query box: 128 rows x 64 columns
       int last[XST] = {-1, -1};
       mbar_arrive_expect_tx(XB(I_Q), box * nd * (uint32_t)a.slots);
       for (int sl = 0; sl < a.slots; ++sl)
@@ -138,11 +143,11 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         if (use > 0 && !mbar_wait(XB(I_KE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
                                   (R_PROD << 8) | (I_KE + st)))
           break;
-        mbar_arrive_expect_tx(XB(I_KF + st), 2u * box * nd);
+        mbar_arrive_expect_tx(XB(I_KF + st), 2u * PBOX * nd);
         for (int c = 0; c < nd; ++c) {
-          tma_load_4d(sb + X_K + 65536u * st + box * c, &maps.hi, XB(I_KF + st), 64 * c, pt * kTile, g, b);
-          tma_load_4d(sb + X_K + 65536u * st + 32768u + box * c, &maps.lo, XB(I_KF + st), 64 * c,
-                      pt * kTile, g, b);
+          tma_load_4d(sb + X_K + 65536u * st + PBOX * c, &maps.hi, XB(I_KF + st), 64 * c, pt * PT, g, b);
+          tma_load_4d(sb + X_K + 65536u * st + 32768u + PBOX * c, &maps.lo, XB(I_KF + st), 64 * c,
+                      pt * PT, g, b);
         }
         last[st] = use;
       }
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && nsteps > 0) {
-      const uint32_t idesc = make_idesc_f16((uint32_t)a.ab_type, 128, 128, 0);  // -> fp32
+      const uint32_t idesc = make_idesc_f16((uint32_t)a.ab_type, 128, PT, 0);  // -> fp32
       const int kq = a.d / 16;
       const uint64_t dq0 = make_sdesc_sw128(sb + X_Q, 16, 1024);
       const uint64_t dk0 = make_sdesc_sw128(sb + X_K, 16, 1024);
@@ -179,17 +184,19 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           const uint64_t bh = dk0 + ((65536u * st) >> 4);
           const uint64_t bl = dk0 + ((65536u * st + 32768u) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
             if (kk < kq) {
-              const uint32_t off = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-              mma_ss(d_tmem, aq + off, bh + off, idesc, kk > 0 ? 1u : 0u);
+              const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+              const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
+              mma_ss(d_tmem, aq + offa, bh + offb, idesc, kk > 0 ? 1u : 0u);
             }
           }
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
             if (kk < kq) {
-              const uint32_t off = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-              mma_ss(d_tmem, aq + off, bl + off, idesc, 1u);
+              const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+              const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
+              mma_ss(d_tmem, aq + offa, bl + offb, idesc, 1u);
             }
           }
           tc_commit(XB(I_SF + 2 * sl + u));
@@ -221,26 +228,28 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
                     (R_ROW << 8) | (I_SF + 2 * sl + u));
       if (!ok) break;
       tc_fence_after();
-      uint32_t xr[128];
-      tmem_ld128_wait(tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl + 128u * u, xr);
+      uint32_t xr[PT];
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl + 128u * u;
+      if constexpr (PT == 128) tmem_ld128_wait(taddr, xr);
+      else tmem_ld64_wait(taddr, xr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(XB(I_SE + 2 * sl + u));
-      const int lim = ob - pt * kTile;  // columns c < lim are candidates
+      const int lim = ob - pt * PT;  // columns c < lim are candidates
       if (pass == 0) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < PT; ++c)
           if (c < lim) smax = fmaxf(smax, __uint_as_float(xr[c]));
       } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < PT / 32; ++q) {
           uint32_t word = 0u;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int c = 32 * q + i;
             if (c < lim && (__uint_as_float(xr[c]) - smax) * a.scale >= a.log_alpha) word |= 1u << i;
           }
-          const int w = pt * 4 + q;
+          const int w = pt * (PT / 32) + q;
           // keep rules on this word's candidates (blocks below ob): sinks, the local
           // window, the dense tail; then the 32-row query tile's union (a warp's rows are
           // one aligned 32-position tile)
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     }
     if (ok) {
       // words past the pooled tiles: only the diagonal bit
-      for (int w = 4 * np; w < a.words; ++w) {
+      for (int w = (PT / 32) * np; w < a.words; ++w) {
         const uint32_t word = (w == dword) ? dbit : 0u;
         if (valid) bits[w] = word;
       }
@@ -362,15 +371,20 @@ cudaError_t launch_share_group(const IndexArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st) {
+template <bool WIDE>
+cudaError_t launch_index_w(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st) {
   static std::atomic<int> configured[64];
   cudaError_t e =
-      ensure_dynamic_smem(reinterpret_cast<const void*>(index_tc_kernel), X_ALLOC, configured);
+      ensure_dynamic_smem(reinterpret_cast<const void*>(index_tc_kernel<WIDE>), X_ALLOC, configured);
   if (e != cudaSuccess) return e;
   const int grid = a.n_qt * a.n_hp * a.B;
-  index_tc_kernel<<<grid, kIndexThreads, X_ALLOC, st>>>(maps, a);
+  index_tc_kernel<WIDE><<<grid, kIndexThreads, X_ALLOC, st>>>(maps, a);
   ++t_launches;
   return cudaGetLastError();
+}
+
+cudaError_t launch_index(const IndexMaps& maps, const IndexArgs& a, cudaStream_t st) {
+  return a.d == 256 ? launch_index_w<true>(maps, a, st) : launch_index_w<false>(maps, a, st);
 }
 
 }  // namespace pf

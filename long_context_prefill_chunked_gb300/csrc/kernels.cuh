@@ -86,11 +86,13 @@ cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, 
 struct PoolArgs {
   const void* x;
   int B, T, H, d, block, nblk;
+  int cap;               // blocks per (b, h) in the outputs (>= nblk)
+  int blk0;              // first block to pool (the ones before are already pooled)
   long long sb, st, sh;
-  float* out_f32;        // [B, H, nblk, d]
-  void* out_lp;          // [B, H, nblk, d] in the input type, may be null
-  void* out_hi;          // [B, H, nblk, d] 16-bit round of the mean, may be null
-  void* out_lo;          // [B, H, nblk, d] 16-bit round of (mean - hi), may be null
+  float* out_f32;        // [B, H, cap, d]
+  void* out_lp;          // [B, H, cap, d] in the input type, may be null
+  void* out_hi;          // [B, H, cap, d] 16-bit round of the mean, may be null
+  void* out_lo;          // [B, H, cap, d] 16-bit round of (mean - hi), may be null
 };
 cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st);
 

@@ -140,11 +140,16 @@ pf_status map_out(CUtensorMap* m, void* base, pf_dtype dt, int B, int C, int Hq,
   return PF_OK;
 }
 
-// Token-major tensor [B, T, H, d] -> map dims (d, H, T, B), box 64 x 1 x 128.
+// Token-major tensor [B, T, H, d] -> map dims (d, H, T, B), box 64 x 1 x rows (128; K / V
+// tiles of head dim 256 are 64 keys).
 pf_status map_tokens(CUtensorMap* m, const void* base, pf_dtype dt, int B, int T, int H, int d,
-                     const long long s[3], const char* what) {
-  return make_map(m, base, dt, d, H, T, B, s[2], s[1], s[0], 1, 128, what);
+                     const long long s[3], const char* what, uint32_t rows = 128) {
+  return make_map(m, base, dt, d, H, T, B, s[2], s[1], s[0], 1, rows, what);
 }
+
+// Keys per key tile of the attention kernel (and pooled blocks per pooled tile): 64 for head dim
+// 256, whose 128-key tiles would not fit the shared-memory rings, else 128.
+int key_tile(int d) { return d == 256 ? 64 : 128; }
 
 pf_status check_common(const pf_shape* sh, int32_t start_pos) {
   if (sh == nullptr) return fail(PF_EINVAL, "shape is NULL");
@@ -152,7 +157,8 @@ pf_status check_common(const pf_shape* sh, int32_t start_pos) {
     return fail(PF_EINVAL, "B, Hq, Hkv and C must be >= 1 (got %d, %d, %d, %d)", sh->B, sh->Hq,
                 sh->Hkv, sh->C);
   if (sh->Hq % sh->Hkv != 0) return fail(PF_EINVAL, "Hq (%d) must be a multiple of Hkv (%d)", sh->Hq, sh->Hkv);
-  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  if (sh->d != 64 && sh->d != 128 && sh->d != 256)
+    return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128, 256)", sh->d);
   if (sh->in_dtype != PF_F16 && sh->in_dtype != PF_BF16)
     return fail(PF_EUNSUPPORTED, "q/k/v dtype must be f16 or bf16");
   if (sh->out_dtype != PF_F32 && sh->out_dtype != PF_BF16 && sh->out_dtype != PF_F16)
@@ -175,7 +181,9 @@ void fill_attn_common(const pf_shape* sh, int32_t start_pos, AttnArgs& a) {
   a.s = start_pos;
   a.T = start_pos + sh->C;
   a.n_qt = (sh->C + kTile - 1) / kTile;
-  a.slots = (a.G % 2 == 0) ? 2 : 1;
+  // two query heads of a KV group share each K / V tile; head dim 256 runs one head per CTA
+  // (its 64 KB query tile fills both slots' room)
+  a.slots = (a.G % 2 == 0 && sh->d != 256) ? 2 : 1;
   a.n_hp = sh->Hq / a.slots;
   a.ab_type = sh->in_dtype == PF_BF16 ? 1 : 0;
   a.convert_v = a.ab_type;
@@ -233,7 +241,8 @@ void plan_split(AttnArgs& a, int mode, void* ws) {
   if (P <= 0 || ws == nullptr) return;
   const int W = (U < P) ? U : U % P;
   if (W == 0 || W > (int)(kCountBytes / 4)) return;
-  const int min_tiles = (mode == MODE_CAUSAL) ? a.s / kTile + 1 : (a.T + kTile - 1) / kTile;
+  const int kt = key_tile(a.d);
+  const int min_tiles = (mode == MODE_CAUSAL) ? (a.s / kTile + 1) * (kTile / kt) : (a.T + kt - 1) / kt;
   int k = P / W;
   if (k > kMaxSplit) k = kMaxSplit;
   if (k > min_tiles / kMinPartTiles) k = min_tiles / kMinPartTiles;
@@ -320,7 +329,7 @@ pf_status dense_entry(const pf_shape* sh, const void* q, const void* k_hist, con
 
   AttnArgs a{};
   fill_attn_common(sh, start_pos, a);
-  a.n_hist_tiles = s / kTile;
+  a.n_hist_tiles = s / key_tile(d);
   a.out = out;
   a.lse = lse;
   a.o_sb = os[0];
@@ -340,11 +349,12 @@ pf_status dense_entry(const pf_shape* sh, const void* q, const void* k_hist, con
   AttnMaps maps;
   const pf_dtype dt = sh->in_dtype;
   if ((rc = map_tokens(&maps.q, q, dt, B, C, Hq, d, qs, "q")) != PF_OK) return rc;
-  if ((rc = map_tokens(&maps.kc, k_chunk, dt, B, C, Hkv, d, kcs, "k_chunk")) != PF_OK) return rc;
-  if ((rc = map_tokens(&maps.vc, v_chunk, dt, B, C, Hkv, d, kcs, "v_chunk")) != PF_OK) return rc;
+  const uint32_t kt_rows = (uint32_t)key_tile(d);
+  if ((rc = map_tokens(&maps.kc, k_chunk, dt, B, C, Hkv, d, kcs, "k_chunk", kt_rows)) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.vc, v_chunk, dt, B, C, Hkv, d, kcs, "v_chunk", kt_rows)) != PF_OK) return rc;
   if (s > 0) {
-    if ((rc = map_tokens(&maps.kh, k_hist, dt, B, s, Hkv, d, khs, "k_hist")) != PF_OK) return rc;
-    if ((rc = map_tokens(&maps.vh, v_hist, dt, B, s, Hkv, d, khs, "v_hist")) != PF_OK) return rc;
+    if ((rc = map_tokens(&maps.kh, k_hist, dt, B, s, Hkv, d, khs, "k_hist", kt_rows)) != PF_OK) return rc;
+    if ((rc = map_tokens(&maps.vh, v_hist, dt, B, s, Hkv, d, khs, "v_hist", kt_rows)) != PF_OK) return rc;
   } else {
     maps.kh = maps.kc;
     maps.vh = maps.vc;
@@ -447,7 +457,8 @@ pf_status pf_stream_status(void* stream) {
 
 pf_status pf_dense_workspace_bytes_masked(const pf_shape* sh, int32_t start_pos, int64_t* bytes) {
   if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
-  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  if (sh->d != 64 && sh->d != 128 && sh->d != 256)
+    return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128, 256)", sh->d);
   if (sh->C < 1 || start_pos < 0) return fail(PF_EINVAL, "C >= 1 and start_pos >= 0 required");
   const int P = sm_count();
   if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
@@ -457,7 +468,8 @@ pf_status pf_dense_workspace_bytes_masked(const pf_shape* sh, int32_t start_pos,
 
 pf_status pf_dense_workspace_bytes(const pf_shape* sh, int64_t* bytes) {
   if (sh == nullptr || bytes == nullptr) return fail(PF_EINVAL, "NULL argument");
-  if (sh->d != 64 && sh->d != 128) return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128)", sh->d);
+  if (sh->d != 64 && sh->d != 128 && sh->d != 256)
+    return fail(PF_EUNSUPPORTED, "head dim %d (supported: 64, 128, 256)", sh->d);
   const int P = sm_count();
   if (P <= 0) return fail(PF_ECUDA, "no CUDA device");
   *bytes = dense_workspace_bytes(sh->d, P);
@@ -507,6 +519,20 @@ pf_status pf_sparse_query_sizes(const pf_shape* sh, int32_t start_pos, int32_t b
 
 namespace {
 
+// The pooled layout of a call: blocks per (b, g) in kbar / vbar (cap) and the blocks an earlier
+// call already pooled (p0).
+pf_status pooled_layout(const pf_sel* sel, int32_t start_pos, int32_t block, const pf_sparse_sizes& z,
+                        int* cap, int* p0) {
+  *cap = sel->capacity > 0 ? sel->capacity : (int)z.nblk;
+  if (sel->capacity < 0 || *cap < z.nblk)
+    return fail(PF_EINVAL, "sel capacity %d is below the %lld key blocks of this call", sel->capacity, z.nblk);
+  if (*cap > 2048) return fail(PF_EUNSUPPORTED, "sel capacity %d key blocks (at most 2048)", *cap);
+  *p0 = sel->pooled_blocks;
+  if (*p0 < 0 || *p0 > start_pos / block)
+    return fail(PF_EINVAL, "pooled_blocks %d outside [0, start_pos / block = %d]", *p0, start_pos / block);
+  return PF_OK;
+}
+
 pf_status check_sparse(const pf_shape* sh, int32_t start_pos, int32_t block, long long ks[3],
                        long long qs[3], pf_sparse_sizes* z) {
   pf_status rc = check_common(sh, start_pos);
@@ -547,7 +573,9 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = start_pos + sh->C;
   const int B = sh->B, Hkv = sh->Hkv, d = sh->d, nblk = (int)z.nblk;
-  const long long pe = z.kbar_elems / 2;
+  int cap = 0, p0 = 0;
+  if ((rc = pooled_layout(sel, start_pos, block, z, &cap, &p0)) != PF_OK) return rc;
+  const long long pe = (long long)B * Hkv * cap * d;  // pooled elements at this capacity
   uint16_t* kb_hi = reinterpret_cast<uint16_t*>(sel->kbar + pe);
   uint16_t* kb_lo = kb_hi + pe;
   PoolArgs p{};
@@ -558,6 +586,8 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
   p.d = d;
   p.block = block;
   p.nblk = nblk;
+  p.cap = cap;
+  p.blk0 = p0;
   p.sb = ks[0];
   p.st = ks[1];
   p.sh = ks[2];
@@ -579,7 +609,7 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
   ia.nblk = nblk;
   ia.n_qt = (int)z.nqt;
   ia.words = (int)z.words;
-  ia.slots = (ia.G % 2 == 0) ? 2 : 1;
+  ia.slots = (ia.G % 2 == 0 && d != 256) ? 2 : 1;
   ia.n_hp = sh->Hq / ia.slots;
   ia.scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)d);
   ia.log_alpha = alpha > 0.f ? logf(alpha) : -INFINITY;
@@ -594,12 +624,13 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
   ia.timeout = g_timeout;
   if (ia.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
   IndexMaps maps;
-  const long long pst[3] = {(long long)Hkv * nblk * d, (long long)nblk * d, (long long)d};
+  const long long pst[3] = {(long long)Hkv * cap * d, (long long)cap * d, (long long)d};
   if ((rc = map_tokens(&maps.q, q, sh->in_dtype, B, sh->C, sh->Hq, d, qs, "q")) != PF_OK) return rc;
-  if ((rc = make_map(&maps.hi, kb_hi, sh->in_dtype, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+  const uint32_t pt_rows = (uint32_t)key_tile(d);  // pooled blocks per pooled tile
+  if ((rc = make_map(&maps.hi, kb_hi, sh->in_dtype, d, nblk, Hkv, B, pst[2], pst[1], pst[0], pt_rows, 1,
                      "kbar hi")) != PF_OK)
     return rc;
-  if ((rc = make_map(&maps.lo, kb_lo, sh->in_dtype, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+  if ((rc = make_map(&maps.lo, kb_lo, sh->in_dtype, d, nblk, Hkv, B, pst[2], pst[1], pst[0], pt_rows, 1,
                      "kbar lo")) != PF_OK)
     return rc;
   if ((e = launch_index(maps, ia, st)) != cudaSuccess) return cuda_fail(e, "index launch");
@@ -628,7 +659,9 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   if (!strides_ok(os, esize(sh->out_dtype))) return fail(PF_EINVAL, "out strides must be multiples of 16 bytes");
   const int B = sh->B, C = sh->C, Hq = sh->Hq, Hkv = sh->Hkv, d = sh->d, T = start_pos + C;
   const int nblk = (int)z.nblk;
-  const long long pe = z.kbar_elems / 2;
+  int cap = 0, p0 = 0;
+  if ((rc = pooled_layout(sel, start_pos, block, z, &cap, &p0)) != PF_OK) return rc;
+  const long long pe = (long long)B * Hkv * cap * d;  // pooled elements at this capacity
   const long long f32b = (pe * 4 + 255) / 256 * 256;
   const long long lpb = (pe * 2 + 255) / 256 * 256;
   float* vbar = static_cast<float*>(pooled);
@@ -645,6 +678,8 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   p.d = d;
   p.block = block;
   p.nblk = nblk;
+  p.cap = cap;
+  p.blk0 = p0;
   p.sb = ks[0];
   p.st = ks[1];
   p.sh = ks[2];
@@ -672,15 +707,16 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
 
   AttnMaps maps;
   const pf_dtype dt = sh->in_dtype;
-  const long long pst[3] = {(long long)Hkv * nblk * d, (long long)nblk * d, (long long)d};
+  const long long pst[3] = {(long long)Hkv * cap * d, (long long)cap * d, (long long)d};
   if ((rc = map_tokens(&maps.q, q, dt, B, C, Hq, d, qs, "q")) != PF_OK) return rc;
-  if ((rc = map_tokens(&maps.kh, k, dt, B, T, Hkv, d, ks, "k")) != PF_OK) return rc;
-  if ((rc = map_tokens(&maps.vh, v, dt, B, T, Hkv, d, ks, "v")) != PF_OK) return rc;
+  const uint32_t kt_rows = (uint32_t)key_tile(d);
+  if ((rc = map_tokens(&maps.kh, k, dt, B, T, Hkv, d, ks, "k", kt_rows)) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.vh, v, dt, B, T, Hkv, d, ks, "v", kt_rows)) != PF_OK) return rc;
   // pooled [B, Hkv, nblk, d]: dims (d, nblk, Hkv, B), box 64 x 128 pooled rows
-  if ((rc = make_map(&maps.kbar, kbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+  if ((rc = make_map(&maps.kbar, kbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], kt_rows, 1,
                      "kbar")) != PF_OK)
     return rc;
-  if ((rc = make_map(&maps.vbar, vbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], 128, 1,
+  if ((rc = make_map(&maps.vbar, vbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], kt_rows, 1,
                      "vbar")) != PF_OK)
     return rc;
   maps.kc = maps.kh;

@@ -80,14 +80,23 @@ pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void
   pf_sparse_sizes z;
   pf_status rc = pf_sparse_query_sizes(shape, start_pos, block, &z);
   if (rc != PF_OK) return rc;
+  if (sel != nullptr && sel->pooled_blocks != 0) {
+    pf::set_error_message("pf_attn_sparse_static: pooled_blocks must be 0 (the shared scratch cannot carry "
+                          "one prompt's pooled blocks from call to call)");
+    return PF_EUNSUPPORTED;
+  }
+  // the scratch covers sel->capacity blocks (nblk when 0)
+  const long long cap = (sel != nullptr && sel->capacity > z.nblk) ? sel->capacity : z.nblk;
+  const long long pe = (long long)shape->B * shape->Hkv * cap * shape->d;
+  const long long need = (pe * 4 + 255) / 256 * 256 + 2 * ((pe * 2 + 255) / 256 * 256);
   // the same size in floating point: a product past int64 shows up here as too large
-  const double approx = (double)shape->B * shape->Hkv * (double)z.nblk * shape->d * 8.0;
-  if (approx > (double)kScratchBytes * 2.0 || z.pooled_bytes < 0 || (size_t)z.pooled_bytes > kScratchBytes) {
+  const double approx = (double)shape->B * shape->Hkv * (double)cap * shape->d * 8.0;
+  if (approx > (double)kScratchBytes * 2.0 || need < 0 || (size_t)need > kScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
              "pf_attn_sparse_static: this problem needs %lld bytes of scratch but the static buffer "
              "holds %zu; use pf_attn_sparse with a caller-allocated workspace",
-             (long long)z.pooled_bytes, kScratchBytes);
+             need, kScratchBytes);
     pf::set_error_message(msg);
     return PF_EUNSUPPORTED;
   }

@@ -26,12 +26,12 @@ __device__ __forceinline__ void unpack8(const uint4 w, bool bf16, float (&f)[8])
   }
 }
 
-// One CTA per (key block, batch); thread t owns 8 consecutive elements of the
-// [H, d] slab of every row of the block and sums them in fp32.
+// One CTA per (key block, batch), blocks blk0 .. nblk - 1; thread t owns 8 consecutive
+// elements of the [H, d] slab of every row of the block and sums them in fp32.
 __global__ void pool_kernel(PoolArgs a, int bf16) {
   const int e0 = threadIdx.x * 8;
   const int h = e0 / a.d, e = e0 % a.d;
-  const int blk = blockIdx.x, b = blockIdx.y;
+  const int blk = a.blk0 + (int)blockIdx.x, b = blockIdx.y;
   const int r0 = blk * a.block;
   const int n = min(a.T - r0, a.block);
   const uint16_t* base = static_cast<const uint16_t*>(a.x) + b * a.sb + (long long)r0 * a.st +
@@ -57,7 +57,7 @@ __global__ void pool_kernel(PoolArgs a, int bf16) {
     for (int k = 0; k < 8; ++k) acc[k] += f[k];
   }
   const float inv = 1.f / (float)n;
-  const long long o = (((long long)b * a.H + h) * a.nblk + blk) * a.d + e;
+  const long long o = (((long long)b * a.H + h) * a.cap + blk) * a.d + e;
   float4* of = reinterpret_cast<float4*>(a.out_f32 + o);
   of[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
   of[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
@@ -154,7 +154,8 @@ cudaError_t launch_order_units(const OrderArgs& o, cudaStream_t st) {
 }
 
 cudaError_t launch_pool(const PoolArgs& a, int bf16, cudaStream_t st) {
-  dim3 grid(a.nblk, a.B);
+  if (a.blk0 >= a.nblk) return cudaSuccess;  // every block already pooled
+  dim3 grid(a.nblk - a.blk0, a.B);
   pool_kernel<<<grid, a.H * a.d / 8, 0, st>>>(a, bf16);
   ++t_launches;
   return cudaGetLastError();

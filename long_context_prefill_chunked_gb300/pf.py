@@ -54,7 +54,8 @@ class Shape(ctypes.Structure):
 
 class Sel(ctypes.Structure):
     _fields_ = [("row_bits", ctypes.c_void_p), ("tile_list", ctypes.c_void_p),
-                ("tile_cnt", ctypes.c_void_p), ("kbar", ctypes.c_void_p)]
+                ("tile_cnt", ctypes.c_void_p), ("kbar", ctypes.c_void_p),
+                ("capacity", ctypes.c_int32), ("pooled_blocks", ctypes.c_int32)]
 
 
 class KeepRules(ctypes.Structure):
@@ -150,7 +151,12 @@ def _expect_selection(sel, z, B, C, Hq, Hkv, d, device):
     _expect(sel.row_bits, (B, Hq, C, z.words), "sel.row_bits", device)
     _expect(sel.tile_list, (B, Hq, z.nqt, z.nblk), "sel.tile_list", device)
     _expect(sel.tile_cnt, (B, Hq, z.nqt), "sel.tile_cnt", device)
-    _expect(sel.kbar, (2, B, Hkv, z.nblk, d), "sel.kbar", device)
+    cap = sel.kbar.shape[3] if sel.kbar.dim() == 5 else -1
+    if cap < z.nblk:
+        raise ValueError("sel.kbar holds %d key blocks, this call needs %d" % (cap, z.nblk))
+    _expect(sel.kbar, (2, B, Hkv, cap, d), "sel.kbar", device)
+    if not sel.kbar.is_contiguous():
+        raise ValueError("sel.kbar must be contiguous")
 
 
 def _expect_lse(lse, B, Hq, C, device):
@@ -314,12 +320,15 @@ def sparse_sizes(q, k, start_pos, block=128) -> SparseSizes:
 @dataclasses.dataclass
 class Selection:
     """Device buffers of a pf_sel: row_bits [B,Hq,C,W] int32 (bit pattern), tile_list
-    [B,Hq,nqt,nblk], tile_cnt [B,Hq,nqt], kbar [2,B,Hkv,nblk,d] fp32 (means, then the
-    library's 16-bit hi/lo split of them)."""
+    [B,Hq,nqt,nblk], tile_cnt [B,Hq,nqt], kbar [2,B,Hkv,cap,d] fp32 (means, then the
+    library's 16-bit hi/lo split of them; cap >= nblk blocks).  pooled_blocks: leading blocks
+    that kbar (and the sparse workspace passed with this selection) already hold from an
+    earlier chunk of the same prompt."""
     row_bits: torch.Tensor
     tile_list: torch.Tensor
     tile_cnt: torch.Tensor
     kbar: torch.Tensor
+    pooled_blocks: int = 0
 
     @property
     def kbar_mean(self) -> torch.Tensor:
@@ -327,18 +336,30 @@ class Selection:
 
     def c_struct(self) -> Sel:
         return Sel(self.row_bits.data_ptr(), self.tile_list.data_ptr(), self.tile_cnt.data_ptr(),
-                   self.kbar.data_ptr())
+                   self.kbar.data_ptr(), int(self.kbar.shape[3]), int(self.pooled_blocks))
 
 
-def alloc_selection(q, k, start_pos, block=128) -> Selection:
+def alloc_kbar(q, k, max_keys, block=128) -> torch.Tensor:
+    """A pooled-key buffer for a prompt of up to max_keys keys, [2, B, Hkv, ceil(max_keys /
+    block), d] fp32: one buffer can serve every chunk of the prompt."""
+    B, d, Hkv = q.shape[0], q.shape[3], k.shape[2]
+    nblk = (int(max_keys) + block - 1) // block
+    return torch.empty((2, B, Hkv, nblk, d), dtype=torch.float32, device=q.device)
+
+
+def alloc_selection(q, k, start_pos, block=128, kbar=None, pooled_blocks=0) -> Selection:
+    """Buffers for pf_block_index on this chunk.  kbar: a shared pooled-key buffer (alloc_kbar)
+    that already holds the first pooled_blocks blocks of this prompt; None allocates one."""
     z = sparse_sizes(q, k, start_pos, block)
     B, C, Hq, d = q.shape
     Hkv = k.shape[2]
     dev = q.device
+    if kbar is None:
+        kbar = torch.empty((2, B, Hkv, z.nblk, d), dtype=torch.float32, device=dev)
     return Selection(torch.empty((B, Hq, C, z.words), dtype=torch.int32, device=dev),
                      torch.empty((B, Hq, z.nqt, z.nblk), dtype=torch.int32, device=dev),
                      torch.empty((B, Hq, z.nqt), dtype=torch.int32, device=dev),
-                     torch.empty((2, B, Hkv, z.nblk, d), dtype=torch.float32, device=dev))
+                     kbar, int(pooled_blocks))
 
 
 def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stream=None,
@@ -361,7 +382,11 @@ def block_index(q, k, start_pos, block=128, alpha=0.1, sel=None, scale=0.0, stre
     return sel
 
 
-def alloc_pooled(q, k, start_pos, block=128) -> torch.Tensor:
+def alloc_pooled(q, k, start_pos, block=128, max_keys=None) -> torch.Tensor:
+    """The pf_attn_sparse workspace; with max_keys, sized for a whole prompt of that many keys
+    (to be shared by its chunks, together with a kbar from alloc_kbar(max_keys))."""
+    if max_keys is not None:  # the sizes depend on the keys' count, not on k's contents
+        start_pos = int(max_keys) - q.shape[1]
     z = sparse_sizes(q, k, start_pos, block)
     return torch.empty((z.pooled_bytes,), dtype=torch.uint8, device=q.device)
 
@@ -380,6 +405,10 @@ def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=
     _expect(v, (B, start_pos + C, Hkv, d), "v", dev)
     z = sparse_sizes(q, k, start_pos, block)
     _expect_selection(sel, z, B, C, Hq, Hkv, d, dev)
+    cap = sel.kbar.shape[3]
+    if cap != z.nblk:  # a workspace shared by a prompt's chunks is sized for its capacity
+        pe = B * Hkv * cap * d
+        z.pooled_bytes = (pe * 4 + 255) // 256 * 256 + 2 * ((pe * 2 + 255) // 256 * 256)
     if out is None:
         out = torch.empty((B, C, Hq, d), dtype=out_dtype, device=q.device)
     _expect(out, (B, C, Hq, d), "out", dev)
@@ -399,12 +428,13 @@ def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=
     return out
 
 
-def vbar_view(pooled: torch.Tensor, q, k, start_pos, block=128) -> torch.Tensor:
-    """The fp32 block means of v at the head of the sparse workspace, [B, Hkv, nblk, d]."""
+def vbar_view(pooled: torch.Tensor, q, k, start_pos, block=128, capacity=None) -> torch.Tensor:
+    """The fp32 block means of v at the head of the sparse workspace, [B, Hkv, cap, d] (cap =
+    capacity, else this call's block count)."""
     z = sparse_sizes(q, k, start_pos, block)
     B, Hkv, d = q.shape[0], k.shape[2], q.shape[3]
-    n = z.kbar_elems // 2  # pooled elements (kbar_elems also counts the 16-bit split)
-    return pooled[: n * 4].view(torch.float32).view(B, Hkv, z.nblk, d)
+    cap = z.nblk if capacity is None else int(capacity)
+    return pooled[: B * Hkv * cap * d * 4].view(torch.float32).view(B, Hkv, cap, d)
 
 
 def stream_status(stream=None):

@@ -58,6 +58,7 @@ def dense(lib, sh, q=FAKE, kh=None, vh=None, kc=FAKE, vc=FAKE, mask=None, s=0, o
 
 @pytest.mark.parametrize("kw,code", [
     (dict(d=96), pf.PF_EUNSUPPORTED),
+    (dict(d=512), pf.PF_EUNSUPPORTED),
     (dict(Hq=6, Hkv=4), pf.PF_EINVAL),
     (dict(C=0), pf.PF_EINVAL),
     (dict(in_dtype=pf.PF_F32), pf.PF_EUNSUPPORTED),
@@ -116,6 +117,21 @@ def test_sparse_rejects_bad_arguments(lib):
     assert lib.pf_attn_sparse(ctypes.byref(sh), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), None, FAKE, None, None) == pf.PF_EINVAL
     long = shape(C=300000)
     assert lib.pf_attn_sparse(ctypes.byref(long), FAKE, FAKE, FAKE, 0, 128, ctypes.byref(sel), FAKE, FAKE, None, None) == pf.PF_EUNSUPPORTED
+
+
+def test_sparse_pooled_reuse_arguments(lib):
+    """capacity below the call's block count, or pooled_blocks beyond the whole history blocks
+    (or negative), is PF_EINVAL for both sparse calls, before anything is launched."""
+    sh = shape(C=256)                                           # start_pos 512: nblk 6, 4 history blocks
+    for cap, pooled in ((5, 0), (-1, 0), (8, 5), (8, -1)):
+        sel = pf.Sel(0x100000, 0x100000, 0x100000, 0x100000, cap, pooled)
+        assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 512, 128, 0.1, None, ctypes.byref(sel),
+                                  None) == pf.PF_EINVAL, (cap, pooled)
+        assert lib.pf_attn_sparse(ctypes.byref(sh), FAKE, FAKE, FAKE, 512, 128, ctypes.byref(sel), FAKE, FAKE,
+                                  None, None) == pf.PF_EINVAL, (cap, pooled)
+    big = pf.Sel(0x100000, 0x100000, 0x100000, 0x100000, 4096, 0)
+    assert lib.pf_block_index(ctypes.byref(sh), FAKE, FAKE, 512, 128, 0.1, None, ctypes.byref(big),
+                              None) == pf.PF_EUNSUPPORTED
 
 
 def test_sparse_sizes(lib):
@@ -229,3 +245,14 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
+
+
+def test_package_exports_every_binding_function():
+    """Every public function of the binding module is reachable from the package."""
+    import inspect
+    import long_context_prefill_chunked_gb300 as pkg
+    from long_context_prefill_chunked_gb300 import pf as mod
+    public = [n for n, f in vars(mod).items() if inspect.isfunction(f) and not n.startswith("_")
+              and f.__module__ == mod.__name__ and n != "make_shape"]
+    missing = [n for n in public if not hasattr(pkg, n)]
+    assert not missing, missing

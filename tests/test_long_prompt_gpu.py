@@ -9,7 +9,8 @@ every 128-row query tile, each with all 32 query heads.  Block-sparse rows are a
 compared, near-threshold rows included: a GPU row selection may differ from the
 oracle's only at near-threshold pairs, and where it does the expected output is the
 oracle's under that (equally valid) selection.  The oracle runs in a pool of worker
-processes, one task per (chunk, KV head, path).
+processes, one task per (chunk, KV head, path).  The sparse path keeps one pooled-key buffer
+and one workspace for the whole prompt, so each chunk pools only its own blocks.
 """
 import numpy as np
 import pytest
@@ -65,6 +66,10 @@ def test_config5_every_chunk_dense_and_sparse(tmp_path):
     Q, K, V = dev(w.q, w.dtype), dev(w.k, w.dtype), dev(w.v, w.dtype)
     cache_k = torch.empty((1, Hkv, N, d), dtype=Q.dtype, device="cuda")
     cache_v = torch.empty_like(cache_k)
+    # the pooled keys and values of the history are kept from chunk to chunk: one buffer each
+    # for the whole prompt, and every call pools only its own chunk's blocks
+    kbar = pfx.alloc_kbar(Q[:, :CH], K, N)
+    pooled = pfx.alloc_pooled(Q[:, :CH], K, 0, max_keys=N)
     tasks = []
     kept_tiles = cand_tiles = 0.0
     for c, s in enumerate(w.starts):
@@ -73,8 +78,9 @@ def test_config5_every_chunk_dense_and_sparse(tmp_path):
         q = Q[:, s:s + CH]
         out_d = pfx.attn_dense(q, K[:, :s], V[:, :s], K[:, s:s + CH], V[:, s:s + CH], s,
                                out_k=cache_k[:, :, s:s + CH], out_v=cache_v[:, :, s:s + CH])
-        sel = pfx.block_index(q, K[:, :s + CH], s, w.block, w.alpha)
-        out_s = pfx.attn_sparse(q, K[:, :s + CH], V[:, :s + CH], s, sel)
+        sel = pfx.alloc_selection(q, K[:, :s + CH], s, kbar=kbar, pooled_blocks=s // w.block)
+        pfx.block_index(q, K[:, :s + CH], s, w.block, w.alpha, sel=sel)
+        out_s = pfx.attn_sparse(q, K[:, :s + CH], V[:, :s + CH], s, sel, pooled=pooled)
         pfx.stream_status()
         oracle_pool.save_result(root, "dense", s, rows, out_d[0, ridx].cpu().numpy())
         oracle_pool.save_result(root, "sparse", s, rows, out_s[0, ridx].cpu().numpy(),
@@ -91,7 +97,7 @@ def test_config5_every_chunk_dense_and_sparse(tmp_path):
     # the cache holds every chunk's K/V, bit for bit
     assert torch.equal(cache_k[0].transpose(0, 1), K[0])
     assert torch.equal(cache_v[0].transpose(0, 1), V[0])
-    del Q, K, V, cache_k, cache_v
+    del Q, K, V, cache_k, cache_v, kbar, pooled
     torch.cuda.empty_cache()
     # planted structure: the executed (tile-union) skip share over the whole prompt
     share = 1.0 - kept_tiles / cand_tiles

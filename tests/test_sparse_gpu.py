@@ -202,6 +202,32 @@ def test_sparse_lse_matches_oracle(small):
         assert np.max(np.abs(got - rlse)) <= tol, (alpha, np.max(np.abs(got - rlse)), tol)
 
 
+def test_chunked_prompt_shares_pooled_blocks(small):
+    """A prompt processed in chunks with one pooled-key buffer and one workspace for all of them
+    (each call pools only the blocks the earlier chunks have not) gives bit-identical selections,
+    pooled means and outputs to fresh buffers per chunk, and matches the oracle."""
+    w = small
+    N, CH = w.N, 512
+    Q, K, V = dev(w.q, w.dtype), dev(w.k, w.dtype), dev(w.v, w.dtype)
+    kbar = pfx.alloc_kbar(Q[:, :CH], K, N)
+    pooled = pfx.alloc_pooled(Q[:, :CH], K, 0, max_keys=N)
+    for s in range(0, N, CH):
+        q, k, v = Q[:, s:s + CH], K[:, :s + CH], V[:, :s + CH]
+        sel_r = pfx.alloc_selection(q, k, s, kbar=kbar, pooled_blocks=s // 128)
+        pfx.block_index(q, k, s, 128, 0.1, sel=sel_r)
+        out_r = pfx.attn_sparse(q, k, v, s, sel_r, pooled=pooled)
+        sel_f = pfx.block_index(q, k, s, 128, 0.1)
+        out_f = pfx.attn_sparse(q, k, v, s, sel_f)
+        pfx.stream_status()
+        nb = (s + CH + 127) // 128
+        assert torch.equal(kbar[0][:, :, :nb], sel_f.kbar[0])
+        assert torch.equal(sel_r.row_bits, sel_f.row_bits) and torch.equal(sel_r.tile_cnt, sel_f.tile_cnt)
+        assert torch.equal(out_r, out_f)
+    rows = np.arange(CH)
+    ref, osel, gk = expected_sparse(w, N - CH, CH, 0.1, rows, sel_r)
+    assert_rows_close(out_r, ref, "chunked with shared pooled blocks")
+
+
 # --------------------------------------------------------------------------- keep rules
 RULES = [
     ("sinks-window", dict(sink_tokens=256, local_blocks=1)),
