@@ -861,9 +861,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // One CTA per mask row (rows past 65535 loop): warp-wide loads of 32 consecutive values
-// become one word through a ballot; the row's kept count decides whether a fully dropped row
-// (a plain softmax over the raw scores with values, NaN with bits) forces the value path; the
-// key tiles the row keeps are ORed into its query tile's tile bitmap (when tiles != null).
+// become one word through a ballot; each warp loads kPackUnroll consecutive words before it
+// ballots them, so that many loads are in flight (the pass is bound by reading the mask); the
+// row's kept count decides whether a fully dropped row (a plain softmax over the raw scores with
+// values, NaN with bits) forces the value path; the key tiles the row keeps are ORed into its
+// query tile's tile bitmap (when tiles != null).
+constexpr int kPackUnroll = 8;
 __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__ mask, int f16, int C,
                                                         int T, long long ld, uint32_t* __restrict__ bits,
                                                         int words, int* nonbinary, uint32_t* tiles,
@@ -871,26 +874,37 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__
   __shared__ int kept_any;
   __shared__ uint32_t row_tiles[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x / 32;
   for (int row = blockIdx.y; row < C; row += gridDim.y) {
     if (threadIdx.x == 0) kept_any = 0;
     for (int t = threadIdx.x; t < 64; t += blockDim.x) row_tiles[t] = 0u;
     __syncthreads();
     bool nonbin = false, any = false;
-    for (int w = warp; w < words; w += blockDim.x / 32) {
-      const int key = w * 32 + lane;
-      bool keep = false;
-      if (key < T) {
-        const long long o = (long long)row * ld + key;
-        const float v = f16 ? __half2float(reinterpret_cast<const __half*>(mask)[o])
-                            : reinterpret_cast<const float*>(mask)[o];
-        keep = v == 0.f;
-        nonbin |= !(v == 0.f || v <= -10000.f);
+    for (int w0 = warp * kPackUnroll; w0 < words; w0 += nwarps * kPackUnroll) {
+      float v[kPackUnroll];
+#pragma unroll
+      for (int u = 0; u < kPackUnroll; ++u) {  // every load first, then the ballots
+        const int key = (w0 + u) * 32 + lane;
+        v[u] = 0.f;
+        if (w0 + u < words && key < T) {
+          const long long o = (long long)row * ld + key;
+          v[u] = f16 ? __half2float(reinterpret_cast<const __half*>(mask)[o])
+                     : reinterpret_cast<const float*>(mask)[o];
+        }
       }
-      const uint32_t word = __ballot_sync(0xffffffffu, keep);
-      any |= word != 0u;
-      if (lane == 0) {
-        bits[(long long)row * words + w] = word;
-        if (tiles != nullptr && word != 0u) atomicOr(&row_tiles[(w >> 2) >> 5], 1u << ((w >> 2) & 31));
+#pragma unroll
+      for (int u = 0; u < kPackUnroll; ++u) {
+        const int w = w0 + u;
+        if (w >= words) break;  // uniform across the warp
+        const bool inb = w * 32 + lane < T;
+        const bool keep = inb && v[u] == 0.f;
+        nonbin |= inb && !(v[u] == 0.f || v[u] <= -10000.f);
+        const uint32_t word = __ballot_sync(0xffffffffu, keep);
+        any |= word != 0u;
+        if (lane == 0) {
+          bits[(long long)row * words + w] = word;
+          if (tiles != nullptr && word != 0u) atomicOr(&row_tiles[(w >> 2) >> 5], 1u << ((w >> 2) & 31));
+        }
       }
     }
     if (__any_sync(0xffffffffu, any) && lane == 0) kept_any = 1;

@@ -39,7 +39,8 @@ constexpr int kMaxWords = 64;
 
 enum {
   I_Q = 0,
-  I_KF = 1,            // hi/lo tile landed, per stage
+  I_QE = 1,            // the unit's MMAs are done reading its Q tile (the next one may load)
+  I_KF = 2,            // hi/lo tile landed, per stage
   I_KE = I_KF + XST,   // stage free (both slots' MMAs on it done)
   I_SF = I_KE + XST,   // score buffer full, per (slot, buffer)
   I_SE = I_SF + 4,     // score buffer drained by the row threads, per (slot, buffer)
@@ -76,6 +77,33 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 
 // WIDE: head dim 256 -- pooled tiles of 64 blocks (hi and lo tiles keep the 32 KB size), one
 // query head per CTA (its 64 KB query tile fills both slots' room).
+// One unit = (batch, 128-row query tile, `slots` query heads of one KV group).  The grid holds at
+// most one CTA per SM and each CTA runs units blockIdx.x, blockIdx.x + gridDim.x, ... (heaviest
+// first): tensor memory and barriers are set up once, the pooled-tile ring and the score buffers
+// keep their phases from unit to unit, and the next unit's Q tile is loaded as soon as the
+// previous unit's last MMA has read Q (I_QE), while its rows are still being thresholded.
+struct IndexUnit {
+  int b, h0, g, qt, q0, ob, np, nsteps;
+};
+
+template <int PT>
+__device__ __forceinline__ IndexUnit index_unit(const IndexArgs& a, int u) {
+  IndexUnit x;
+  const int per_qt = a.n_hp * a.B;
+  x.qt = a.n_qt - 1 - u / per_qt;
+  const int rem = u % per_qt;
+  x.b = rem / a.n_hp;
+  x.h0 = (rem % a.n_hp) * a.slots;
+  x.g = x.h0 / a.G;
+  x.q0 = x.qt * kTile;
+  x.ob = (a.s + x.q0) / kTile;        // diagonal block; candidates 0 .. ob-1
+  x.np = (x.ob + PT - 1) / PT;        // pooled tiles holding the candidates
+  x.nsteps = 2 * x.np;                // pass 1 and pass 2
+  return x;
+}
+
+// WIDE: head dim 256 -- pooled tiles of 64 blocks (hi and lo tiles keep the 32 KB size), one
+// query head per CTA (its 64 KB query tile fills both slots' room).
 template <bool WIDE>
 __global__ void __launch_bounds__(kIndexThreads, 1)
     index_tc_kernel(const __grid_constant__ IndexMaps maps, const IndexArgs a) {
@@ -91,20 +119,11 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + X_BAR + 8 * I_N);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + X_BAR + 8 * I_N + 4);
   uint32_t* uni = reinterpret_cast<uint32_t*>(smem + X_UNI);  // [slot][64]
-
-  const int per_qt = a.n_hp * a.B;
-  const int qt = a.n_qt - 1 - (int)blockIdx.x / per_qt;
-  const int rem = (int)blockIdx.x % per_qt;
-  const int b = rem / a.n_hp;
-  const int h0 = (rem % a.n_hp) * a.slots;
-  const int g = h0 / a.G;
-  const int q0 = qt * kTile;
-  const int ob = (a.s + q0) / kTile;           // diagonal block; candidates 0 .. ob-1
-  const int np = (ob + PT - 1) / PT;           // pooled tiles holding the candidates
-  const int nsteps = 2 * np;                   // pass 1 and pass 2
+  const int n_units = a.n_qt * a.n_hp * a.B;
 
   if (threadIdx.x == 0) {
     mbar_init(XB(I_Q), 1);
+    mbar_init(XB(I_QE), 1);
     for (int st = 0; st < XST; ++st) {
       mbar_init(XB(I_KF + st), 1);
       mbar_init(XB(I_KE + st), 1);
@@ -129,30 +148,42 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
 
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0 && nsteps > 0) {
+    if (lane == 0) {
       const int nd = a.d / 64;
       const uint32_t box = 16384u;  // a query box: 128 rows x 64 columns
       int last[XST] = {-1, -1};
-      mbar_arrive_expect_tx(XB(I_Q), box * nd * (uint32_t)a.slots);
-      for (int sl = 0; sl < a.slots; ++sl)
-        for (int c = 0; c < nd; ++c)
-          tma_load_4d(sb + X_Q + 32768u * sl + box * c, &maps.q, XB(I_Q), 64 * c, h0 + sl, q0, b);
-      for (int t = 0; t < nsteps; ++t) {
-        const int st = t % XST, use = t / XST;
-        const int pt = t % np;
-        if (use > 0 && !mbar_wait(XB(I_KE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
-                                  (R_PROD << 8) | (I_KE + st)))
+      int qloads = 0, last_q = -1;  // Q tiles loaded so far (units with candidates)
+      long long tg = 0;             // ring steps so far, over all units
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const IndexUnit x = index_unit<PT>(a, u);
+        if (x.nsteps == 0) continue;  // no candidate: nothing to score
+        // the previous unit's MMAs must be done reading Q before it is overwritten
+        if (qloads > 0 && !(ok = mbar_wait(XB(I_QE), (uint32_t)(qloads - 1) & 1u, a.timeout, abort_flag,
+                                            a.status, (R_PROD << 8) | I_QE)))
           break;
-        mbar_arrive_expect_tx(XB(I_KF + st), 2u * PBOX * nd);
-        for (int c = 0; c < nd; ++c) {
-          tma_load_4d(sb + X_K + 65536u * st + PBOX * c, &maps.hi, XB(I_KF + st), 64 * c, pt * PT, g, b);
-          tma_load_4d(sb + X_K + 65536u * st + 32768u + PBOX * c, &maps.lo, XB(I_KF + st), 64 * c,
-                      pt * PT, g, b);
+        mbar_arrive_expect_tx(XB(I_Q), box * nd * (uint32_t)a.slots);
+        for (int sl = 0; sl < a.slots; ++sl)
+          for (int c = 0; c < nd; ++c)
+            tma_load_4d(sb + X_Q + 32768u * sl + box * c, &maps.q, XB(I_Q), 64 * c, x.h0 + sl, x.q0, x.b);
+        last_q = qloads++;
+        for (int t = 0; t < x.nsteps; ++t, ++tg) {
+          const int st = (int)(tg % XST), use = (int)(tg / XST);
+          const int pt = t % x.np;
+          if (use > 0 && !(ok = mbar_wait(XB(I_KE + st), (uint32_t)(use - 1) & 1u, a.timeout, abort_flag,
+                                          a.status, (R_PROD << 8) | (I_KE + st))))
+            break;
+          mbar_arrive_expect_tx(XB(I_KF + st), 2u * PBOX * nd);
+          for (int c = 0; c < nd; ++c) {
+            tma_load_4d(sb + X_K + 65536u * st + PBOX * c, &maps.hi, XB(I_KF + st), 64 * c, pt * PT, x.g, x.b);
+            tma_load_4d(sb + X_K + 65536u * st + 32768u + PBOX * c, &maps.lo, XB(I_KF + st), 64 * c,
+                        pt * PT, x.g, x.b);
+          }
+          last[st] = use;
         }
-        last[st] = use;
       }
       if (*abort_flag) {
-        drain_wait(XB(I_Q), 0, a.timeout, a.status);
+        if (last_q >= 0) drain_wait(XB(I_Q), (uint32_t)last_q & 1u, a.timeout, a.status);
         for (int st = 0; st < XST; ++st)
           if (last[st] >= 0) drain_wait(XB(I_KF + st), last[st] & 1, a.timeout, a.status);
       }
@@ -160,49 +191,59 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nsteps > 0) {
+    if (lane == 0) {
       const uint32_t idesc = make_idesc_f16((uint32_t)a.ab_type, 128, PT, 0);  // -> fp32
       const int kq = a.d / 16;
       const uint64_t dq0 = make_sdesc_sw128(sb + X_Q, 16, 1024);
       const uint64_t dk0 = make_sdesc_sw128(sb + X_K, 16, 1024);
-      bool ok = mbar_wait(XB(I_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | I_Q);
-      tc_fence_after();
-      for (int t = 0; ok && t < nsteps; ++t) {
-        const int st = t % XST, u = t % 2;
-        ok = mbar_wait(XB(I_KF + st), (uint32_t)(t / XST) & 1u, a.timeout, abort_flag, a.status,
-                       (R_MMA << 8) | (I_KF + st));
+      bool ok = true;
+      int qloads = 0;
+      long long tg = 0;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const IndexUnit x = index_unit<PT>(a, u);
+        if (x.nsteps == 0) continue;
+        ok = mbar_wait(XB(I_Q), (uint32_t)qloads & 1u, a.timeout, abort_flag, a.status, (R_MMA << 8) | I_Q);
+        ++qloads;
         if (!ok) break;
-        for (int sl = 0; sl < a.slots; ++sl) {
-          if (t >= 2) {
-            ok = mbar_wait(XB(I_SE + 2 * sl + u), (uint32_t)(t / 2 - 1) & 1u, a.timeout, abort_flag,
-                           a.status, (R_MMA << 8) | (I_SE + 2 * sl + u));
-            if (!ok) break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem + 256u * sl + 128u * u;
-          const uint64_t aq = dq0 + ((32768u * sl) >> 4);
-          const uint64_t bh = dk0 + ((65536u * st) >> 4);
-          const uint64_t bl = dk0 + ((65536u * st + 32768u) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
-            if (kk < kq) {
-              const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-              const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
-              mma_ss(d_tmem, aq + offa, bh + offb, idesc, kk > 0 ? 1u : 0u);
+        tc_fence_after();
+        for (int t = 0; ok && t < x.nsteps; ++t, ++tg) {
+          const int st = (int)(tg % XST), ub = (int)(tg % 2);
+          ok = mbar_wait(XB(I_KF + st), (uint32_t)(tg / XST) & 1u, a.timeout, abort_flag, a.status,
+                         (R_MMA << 8) | (I_KF + st));
+          if (!ok) break;
+          for (int sl = 0; sl < a.slots; ++sl) {
+            if (tg >= 2) {
+              ok = mbar_wait(XB(I_SE + 2 * sl + ub), (uint32_t)(tg / 2 - 1) & 1u, a.timeout, abort_flag,
+                             a.status, (R_MMA << 8) | (I_SE + 2 * sl + ub));
+              if (!ok) break;
             }
-          }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + 256u * sl + 128u * ub;
+            const uint64_t aq = dq0 + ((32768u * sl) >> 4);
+            const uint64_t bh = dk0 + ((65536u * st) >> 4);
+            const uint64_t bl = dk0 + ((65536u * st + 32768u) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
-            if (kk < kq) {
-              const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-              const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
-              mma_ss(d_tmem, aq + offa, bl + offb, idesc, 1u);
+            for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
+              if (kk < kq) {
+                const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+                const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
+                mma_ss(d_tmem, aq + offa, bh + offb, idesc, kk > 0 ? 1u : 0u);
+              }
             }
+#pragma unroll
+            for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
+              if (kk < kq) {
+                const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+                const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
+                mma_ss(d_tmem, aq + offa, bl + offb, idesc, 1u);
+              }
+            }
+            tc_commit(XB(I_SF + 2 * sl + ub));
           }
-          tc_commit(XB(I_SF + 2 * sl + u));
+          if (!ok) break;
+          tc_commit(XB(I_KE + st));
         }
-        if (!ok) break;
-        tc_commit(XB(I_KE + st));
+        if (ok) tc_commit(XB(I_QE));  // this unit's MMAs are the last to read its Q
       }
       tc_commit(XB(I_DR));
       drain_wait(XB(I_DR), 0, a.timeout, a.status);
@@ -212,95 +253,105 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     // ---------------------------------------------------------------- row threads
     const int sl = warp >> 2, quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int h = h0 + sl;
-    const int row = q0 + r;
-    const bool valid = row < a.C;
-    uint32_t* bits = a.row_bits + ((long long)(b * a.Hq + h) * a.C + (valid ? row : 0)) * a.words;
     uint32_t* un = uni + kMaxWords * sl;
-    const int dword = ob >> 5;
-    const uint32_t dbit = 1u << (ob & 31);
-    float smax = -INFINITY;
     bool ok = true;
-    const bool tail_row = a.s + row >= a.tail_from;  // dense-tail rule: keep every candidate
-    for (int t = 0; t < nsteps; ++t) {
-      const int u = t % 2, pass = t / np, pt = t % np;
-      ok = wait_all(XB(I_SF + 2 * sl + u), (uint32_t)(t / 2) & 1u, a.timeout, abort_flag, a.status,
-                    (R_ROW << 8) | (I_SF + 2 * sl + u));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t xr[PT];
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl + 128u * u;
-      if constexpr (PT == 128) tmem_ld128_wait(taddr, xr);
-      else tmem_ld64_wait(taddr, xr);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(XB(I_SE + 2 * sl + u));
-      const int lim = ob - pt * PT;  // columns c < lim are candidates
-      if (pass == 0) {
+    long long tg = 0;
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      const IndexUnit x = index_unit<PT>(a, u);
+      const int h = x.h0 + sl;
+      const int row = x.q0 + r;
+      const bool valid = row < a.C;
+      uint32_t* bits = a.row_bits + ((long long)(x.b * a.Hq + h) * a.C + (valid ? row : 0)) * a.words;
+      const int ob = x.ob, np = x.np;
+      const int dword = ob >> 5;
+      const uint32_t dbit = 1u << (ob & 31);
+      float smax = -INFINITY;
+      const bool tail_row = a.s + row >= a.tail_from;  // dense-tail rule: keep every candidate
+      for (int t = 0; t < x.nsteps; ++t, ++tg) {
+        const int ub = (int)(tg % 2), pass = t / np, pt = t % np;
+        ok = wait_all(XB(I_SF + 2 * sl + ub), (uint32_t)(tg / 2) & 1u, a.timeout, abort_flag, a.status,
+                      (R_ROW << 8) | (I_SF + 2 * sl + ub));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t xr[PT];
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl + 128u * ub;
+        if constexpr (PT == 128) tmem_ld128_wait(taddr, xr);
+        else tmem_ld64_wait(taddr, xr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(XB(I_SE + 2 * sl + ub));
+        const int lim = ob - pt * PT;  // columns c < lim are candidates
+        if (pass == 0) {
 #pragma unroll
-        for (int c = 0; c < PT; ++c)
-          if (c < lim) smax = fmaxf(smax, __uint_as_float(xr[c]));
-      } else {
+          for (int c = 0; c < PT; ++c)
+            if (c < lim) smax = fmaxf(smax, __uint_as_float(xr[c]));
+        } else {
 #pragma unroll
-        for (int q = 0; q < PT / 32; ++q) {
-          uint32_t word = 0u;
+          for (int q = 0; q < PT / 32; ++q) {
+            uint32_t word = 0u;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 32 * q + i;
-            if (c < lim && (__uint_as_float(xr[c]) - smax) * a.scale >= a.log_alpha) word |= 1u << i;
+            for (int i = 0; i < 32; ++i) {
+              const int c = 32 * q + i;
+              if (c < lim && (__uint_as_float(xr[c]) - smax) * a.scale >= a.log_alpha) word |= 1u << i;
+            }
+            const int w = pt * (PT / 32) + q;
+            // keep rules on this word's candidates (blocks below ob): sinks, the local
+            // window, the dense tail; then the 32-row query tile's union (a warp's rows are
+            // one aligned 32-position tile)
+            const uint32_t rule = tail_row ? 0xFFFFFFFFu
+                                           : (range_bits(w, 0, a.sink_blocks) |
+                                              range_bits(w, ob - a.local_blocks, ob));
+            word |= rule & range_bits(w, 0, ob);
+            if (a.row_group32) word = __reduce_or_sync(0xffffffffu, valid ? word : 0u);
+            if (w == dword) word |= dbit;
+            if (w < a.words) {
+              if (valid) bits[w] = word;
+              const uint32_t uw = __reduce_or_sync(0xffffffffu, valid ? word : 0u);
+              if (lane == 0 && uw) atomicOr(&un[w], uw);
+            }
           }
-          const int w = pt * (PT / 32) + q;
-          // keep rules on this word's candidates (blocks below ob): sinks, the local
-          // window, the dense tail; then the 32-row query tile's union (a warp's rows are
-          // one aligned 32-position tile)
-          const uint32_t rule = tail_row ? 0xFFFFFFFFu
-                                         : (range_bits(w, 0, a.sink_blocks) |
-                                            range_bits(w, ob - a.local_blocks, ob));
-          word |= rule & range_bits(w, 0, ob);
-          if (a.row_group32) word = __reduce_or_sync(0xffffffffu, valid ? word : 0u);
-          if (w == dword) word |= dbit;
-          if (w < a.words) {
-            if (valid) bits[w] = word;
-            const uint32_t uw = __reduce_or_sync(0xffffffffu, valid ? word : 0u);
-            if (lane == 0 && uw) atomicOr(&un[w], uw);
-          }
         }
       }
-    }
-    if (ok) {
-      // words past the pooled tiles: only the diagonal bit
-      for (int w = (PT / 32) * np; w < a.words; ++w) {
-        const uint32_t word = (w == dword) ? dbit : 0u;
-        if (valid) bits[w] = word;
+      if (ok) {
+        // words past the pooled tiles: only the diagonal bit
+        for (int w = (PT / 32) * np; w < a.words; ++w) {
+          const uint32_t word = (w == dword) ? dbit : 0u;
+          if (valid) bits[w] = word;
+        }
+        if (r == 0) atomicOr(&un[dword], dbit);
       }
-      if (r == 0) atomicOr(&un[dword], dbit);
-    }
-    // the slot's four row warps finish their unions before warp 0 of the slot compacts
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + sl) : "memory");
-    if (quad == 0 && ok) {
-      const long long tl = (long long)(b * a.Hq + h) * a.n_qt + qt;
-      int32_t* list = a.tile_list + tl * a.nblk;
-      int base = 0;
-      for (int w0 = 0; w0 < a.words; w0 += 32) {
-        const int w = w0 + lane;
-        const uint32_t bw = (w < a.words) ? un[w] : 0u;
-        const int cnt = __popc(bw);
-        int incl = cnt;
+      // the slot's four row warps finish their unions before warp 0 of the slot compacts, and
+      // the compaction has read the union before it is cleared for the next unit; a bounded
+      // wait that gave up in any of them ends the unit loop for all four alike
+      if (!named_bar_and(1u + (uint32_t)sl, 128u, ok)) break;
+      if (quad == 0) {
+        const long long tl = (long long)(x.b * a.Hq + h) * a.n_qt + x.qt;
+        int32_t* list = a.tile_list + tl * a.nblk;
+        int base = 0;
+        for (int w0 = 0; w0 < a.words; w0 += 32) {
+          const int w = w0 + lane;
+          const uint32_t bw = (w < a.words) ? un[w] : 0u;
+          const int cnt = __popc(bw);
+          int incl = cnt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          int pos = base + incl - cnt;
+          uint32_t rb = bw;
+          while (rb) {
+            const int i = __ffs(rb) - 1;
+            rb &= rb - 1u;
+            list[pos++] = w * 32 + i;
+          }
+          base += __shfl_sync(0xffffffffu, incl, 31);
         }
-        int pos = base + incl - cnt;
-        uint32_t rb = bw;
-        while (rb) {
-          const int i = __ffs(rb) - 1;
-          rb &= rb - 1u;
-          list[pos++] = w * 32 + i;
-        }
-        base += __shfl_sync(0xffffffffu, incl, 31);
+        if (lane == 0) a.tile_cnt[tl] = base;
       }
-      if (lane == 0) a.tile_cnt[tl] = base;
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + sl) : "memory");
+      for (int w = r; w < kMaxWords; w += 128) un[w] = 0u;
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + sl) : "memory");
     }
   }
   tc_fence_before();
@@ -377,7 +428,8 @@ cudaError_t launch_index_w(const IndexMaps& maps, const IndexArgs& a, cudaStream
   cudaError_t e =
       ensure_dynamic_smem(reinterpret_cast<const void*>(index_tc_kernel<WIDE>), X_ALLOC, configured);
   if (e != cudaSuccess) return e;
-  const int grid = a.n_qt * a.n_hp * a.B;
+  const int units = a.n_qt * a.n_hp * a.B;
+  const int grid = units < a.grid ? units : a.grid;  // at most one CTA per SM; each loops over units
   index_tc_kernel<WIDE><<<grid, kIndexThreads, X_ALLOC, st>>>(maps, a);
   ++t_launches;
   return cudaGetLastError();

@@ -120,6 +120,7 @@ struct IndexArgs {
   int32_t* tile_cnt;
   unsigned* status;
   long long timeout;
+  int grid;              // CTAs to launch (one per SM); each runs units blockIdx.x + k * grid
 };
 struct IndexMaps {
   CUtensorMap q, hi, lo;

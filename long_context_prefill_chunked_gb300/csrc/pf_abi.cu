@@ -622,6 +622,8 @@ pf_status pf_block_index(const pf_shape* sh, const void* q, const void* k, int32
   ia.tile_cnt = sel->tile_cnt;
   ia.status = status_words();
   ia.timeout = g_timeout;
+  ia.grid = sm_count();
+  if (ia.grid <= 0) return fail(PF_ECUDA, "no CUDA device");
   if (ia.status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
   IndexMaps maps;
   const long long pst[3] = {(long long)Hkv * cap * d, (long long)cap * d, (long long)d};

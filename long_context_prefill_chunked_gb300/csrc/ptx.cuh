@@ -83,6 +83,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// As named_bar_sync, and returns whether `pred` held in every participating thread.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // Register rebalancing between warpgroups (all four warps of a warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
