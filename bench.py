@@ -266,6 +266,22 @@ def run_case(args):
     import long_context_prefill_chunked_gb300 as pfx
     import prefill_inputs as pi
     to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    if args.case == "mask-config2":
+        # config 2: three 4096-row chunks (16q/8kv, d128) at starts 0 / 4096 / 8192, each under an
+        # explicit fp32 0 / -30000 causal mask, K/V re-emitted into a head-major cache
+        w2 = pi.config(2)
+        Q, K, V = (to_dev(x) for x in (w2.q, w2.k, w2.v))
+        masks = [torch.from_numpy(pi.causal_mask(w2.chunk, s)).cuda() for s in w2.starts]
+        ck = torch.empty((1, w2.Hkv, w2.N, w2.d), dtype=torch.bfloat16, device="cuda")
+        cv = torch.empty_like(ck)
+
+        def run():
+            for s, m in zip(w2.starts, masks):
+                c = w2.chunk
+                pfx.attn_dense(Q[:, s:s + c], K[:, :s], V[:, :s], K[:, s:s + c], V[:, s:s + c], s, mask=m,
+                               out_k=ck[:, :, s:s + c], out_v=cv[:, :, s:s + c])
+        flops = sum(4.0 * w2.Hq * w2.d * (w2.chunk * s + w2.chunk * (w2.chunk + 1) // 2) for s in w2.starts)
+        return _time_case(args, pfx, run, flops, 0)
     if args.case in ("indexed-config3", "mask-config3"):
         # a 4096-row chunk over an 8192-token history (16q/8kv, d128), 512 compressed blocks of
         # 4 keys kept per query: as keep lists, or folded into an fp32 0 / -30000 mask
@@ -426,6 +442,59 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
     }
 
 
+TRAFFIC_CMD = ("python bench.py --steps 1 --warmup 3 --no-cpu-baseline --no-long --e2e-steps 1 && "
+               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+               "--clock-control none --print-units base --kernel-name-base demangled "
+               "-k 'regex:attn_fwd_kernel<\\(int\\)0' -s 0 -c 8 --csv --log-file traffic.csv "
+               "python bench.py --steps 1 --warmup 3 --no-cpu-baseline --no-long --e2e-steps 1 && "
+               "python bench.py --write-traffic traffic.csv")
+
+
+def write_traffic(csv_path):
+    """Turn the ncu capture of TRAFFIC_CMD (the eight dense causal launches of the first warm-up
+    step, one per 4096-row chunk in order) into profiles/attn_dense_traffic.json, stamped with the
+    kernel sources' hash so that the bench reports it only while the kernel is unchanged."""
+    import csv
+    import re
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9,
+             "ns": 1e-6, "nsecond": 1e-6, "us": 1e-3, "usecond": 1e-3, "ms": 1.0, "msecond": 1.0, "s": 1e3,
+             "second": 1e3}
+    launches = {}
+    with open(csv_path) as fh:
+        rows = [ln for ln in fh if ln.startswith('"')]
+    for r in csv.DictReader(rows):
+        if not re.search(r"attn_fwd_kernel<(\(int\))?0[,>]", r["Kernel Name"]):  # mode 0: causal
+            continue
+        v = float(r["Metric Value"].replace(",", "")) * scale[r["Metric Unit"]]
+        launches.setdefault(int(r["ID"]), {})[r["Metric Name"]] = v
+    ids = sorted(launches)
+    if len(ids) != len(range(0, N_TOK, CHUNK)):
+        raise SystemExit("expected %d dense launches in %s, found %d" % (N_TOK // CHUNK, csv_path, len(ids)))
+    per = []
+    for i, start in zip(ids, range(0, N_TOK, CHUNK)):
+        m = launches[i]
+        # algorithmic: Q, the chunk's K / V and the history's K / V read once (bf16), fp32 O written
+        alg = 2 * CHUNK * HQ * D + 2 * 2 * (start + CHUNK) * HKV * D + 4 * CHUNK * HQ * D
+        per.append({"start": start, "dram_read": int(m["dram__bytes_read.sum"]),
+                    "dram_write": int(m["dram__bytes_write.sum"]), "algorithmic": alg,
+                    "ncu_ms": round(m["gpu__time_duration.sum"], 6)})
+    rec = {
+        "kernel": "attn_fwd_kernel<0> (dense causal)",
+        "workload": "32K prompt, 8 chunks of 4096 rows, 32q/8kv, d128, bf16 in, fp32 out",
+        "bytes_per_launch": int(round(sum(x["dram_read"] + x["dram_write"] for x in per) / len(per))),
+        "source_sha256": kernel_source_hash(),
+        "note": "dram__bytes_read.sum + dram__bytes_write.sum of the 8 causal launches of one step (the "
+                "first warm-up step of the command below), averaged; writes undercount the fp32 output "
+                "because dirty lines can still sit in L2 when the kernel ends",
+        "command": TRAFFIC_CMD,
+        "per_launch": per,
+    }
+    with open(os.path.join(ROOT, "profiles", "attn_dense_traffic.json"), "w") as fh:
+        json.dump(rec, fh, indent=1)
+        fh.write("\n")
+    print(json.dumps({"bytes_per_launch": rec["bytes_per_launch"], "launches": len(per)}))
+
+
 # ---------------------------------------------------------------------------- ours
 def main():
     ap = argparse.ArgumentParser()
@@ -439,15 +508,21 @@ def main():
     ap.add_argument("--no-long", action="store_true", help="skip the 128K-token record")
     ap.add_argument("--long-reps", type=int, default=3)
     ap.add_argument("--case", default="full", choices=["full", "dense-chunk", "sparse", "sparse-shared",
-                                                       "sparse-128k-chunk", "indexed-config3", "mask-config3"],
+                                                       "sparse-128k-chunk", "indexed-config3", "mask-config3",
+                                                       "mask-config2"],
                     help="profiling cases, timings only: dense-chunk (one 4096-row chunk at "
                          "--start, K/V re-emitted into a cache), sparse (the 32K block-sparse pair), "
                          "sparse-shared (the same with KV-group shared selection), sparse-128k-chunk "
                          "(the pair for the last 4096-row chunk of the 128K prompt), indexed-config3 / "
-                         "mask-config3 (config 3's selection as keep lists / as a folded mask)")
+                         "mask-config3 (config 3's selection as keep lists / as a folded mask), "
+                         "mask-config2 (config 2's three chunks under explicit causal masks)")
     ap.add_argument("--start", type=int, default=N_TOK - CHUNK,
                     help="dense-chunk case: the chunk's first token (a multiple of 4096)")
+    ap.add_argument("--write-traffic", metavar="CSV",
+                    help="write profiles/attn_dense_traffic.json from an ncu capture (no GPU work)")
     args = ap.parse_args()
+    if args.write_traffic:
+        return write_traffic(args.write_traffic)
     if args.impl == "reference":
         return run_reference(args)
     if args.case != "full":
