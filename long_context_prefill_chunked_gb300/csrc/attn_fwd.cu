@@ -918,6 +918,100 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__
   }
 }
 
+// The same packing for masks whose rows start on 16-byte boundaries (the common case): each lane
+// reads four consecutive keys with one streaming vector load (16 bytes of fp32, 8 of fp16), so a
+// warp covers one 128-key tile per load and keeps kPackGroups tiles in flight.  Lane L holds keys
+// 4L .. 4L + 3 of the tile, i.e. bits 4(L mod 8) .. 4(L mod 8) + 3 of the tile's word L / 8; three
+// xor-shuffles inside each group of eight lanes assemble the four words, and one vote gives the
+// tile's "some key kept" bit.  Bits, flags and tile bitmap are those of mask_pack_kernel.
+constexpr int kPackGroups = 4;
+// The first n (< 4) mask values from element o on, one scalar load each; the rest 0.  Kept out of
+// line: inlined, its per-key branches cost the packing kernel a stack frame.
+__device__ __noinline__ float4 ragged_keys(const void* mask, int f16, long long o, int n) {
+  float x[3] = {0.f, 0.f, 0.f};
+  for (int c = 0; c < n && c < 3; ++c)
+    x[c] = f16 ? __half2float(static_cast<const __half*>(mask)[o + c]) : static_cast<const float*>(mask)[o + c];
+  return make_float4(x[0], x[1], x[2], 0.f);
+}
+__global__ void __launch_bounds__(256) mask_pack_vec_kernel(const void* __restrict__ mask, int f16, int C,
+                                                            int T, long long ld, uint32_t* __restrict__ bits,
+                                                            int words, int* nonbinary, uint32_t* tiles,
+                                                            int tile_words) {
+  __shared__ int kept_any;
+  __shared__ uint32_t row_tiles[64];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x / 32;
+  const int groups = words / 4;  // 128-key tiles per row (words is a multiple of 4)
+  const int oct = lane & 7;
+  for (int row = blockIdx.y; row < C; row += gridDim.y) {
+    if (threadIdx.x == 0) kept_any = 0;
+    for (int t = threadIdx.x; t < 64; t += blockDim.x) row_tiles[t] = 0u;
+    __syncthreads();
+    bool nonbin = false, any = false;
+    const long long rbase = (long long)row * ld;
+    for (int m0 = warp * kPackGroups; m0 < groups; m0 += nwarps * kPackGroups) {
+      float v[kPackGroups][4];
+#pragma unroll
+      for (int u = 0; u < kPackGroups; ++u) {  // every load first, then the shuffles
+        const int key0 = (m0 + u) * kTile + 4 * lane;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[u][c] = 0.f;
+        if (m0 + u < groups && key0 < T) {
+          if (key0 + 4 <= T) {
+            if (f16) {
+              const uint2 r = __ldcs(reinterpret_cast<const uint2*>(static_cast<const __half*>(mask) + rbase + key0));
+              v[u][0] = __half2float(__ushort_as_half((unsigned short)(r.x & 0xFFFFu)));
+              v[u][1] = __half2float(__ushort_as_half((unsigned short)(r.x >> 16)));
+              v[u][2] = __half2float(__ushort_as_half((unsigned short)(r.y & 0xFFFFu)));
+              v[u][3] = __half2float(__ushort_as_half((unsigned short)(r.y >> 16)));
+            } else {
+              const float4 r = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(mask) + rbase + key0));
+              v[u][0] = r.x;
+              v[u][1] = r.y;
+              v[u][2] = r.z;
+              v[u][3] = r.w;
+            }
+          } else {  // the row's ragged end: only keys below T exist
+            const float4 r = ragged_keys(mask, f16, rbase + key0, T - key0);
+            v[u][0] = r.x;
+            v[u][1] = r.y;
+            v[u][2] = r.z;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPackGroups; ++u) {
+        const int m = m0 + u;
+        if (m >= groups) break;  // uniform across the warp
+        const int key0 = m * kTile + 4 * lane;
+        uint32_t nib = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const bool inb = key0 + c < T;
+          nonbin |= inb && !(v[u][c] == 0.f || v[u][c] <= -10000.f);
+          nib |= (inb && v[u][c] == 0.f) ? (1u << c) : 0u;
+        }
+        uint32_t word = nib << (4 * oct);
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+        if (oct == 0) bits[(long long)row * words + 4 * m + (lane >> 3)] = word;
+        const bool tile_kept = __any_sync(0xffffffffu, nib != 0u);
+        any |= tile_kept;
+        if (lane == 0 && tiles != nullptr && tile_kept) atomicOr(&row_tiles[m >> 5], 1u << (m & 31));
+      }
+    }
+    if (__any_sync(0xffffffffu, any) && lane == 0) kept_any = 1;
+    if (__any_sync(0xffffffffu, nonbin) && lane == 0) atomicExch(nonbinary, 1);
+    __syncthreads();
+    if (threadIdx.x == 0 && !kept_any) atomicExch(nonbinary, 1);
+    if (tiles != nullptr)
+      for (int t = threadIdx.x; t < tile_words; t += blockDim.x)
+        if (row_tiles[t] != 0u) atomicOr(&tiles[(long long)(row / kTile) * tile_words + t], row_tiles[t]);
+    __syncthreads();
+  }
+}
+
 __global__ void kv_relayout_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                    int B, int C, int H, int d, long long s0, long long s1,
                                    long long s2, long long d0, long long d1, long long d2) {
@@ -968,10 +1062,13 @@ cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaS
   }
 }
 
-cudaError_t launch_mask_pack(const void* mask, int f16, int C, int T, long long ld, uint32_t* bits,
+cudaError_t launch_mask_pack(const void* mask, int f16, int vec, int C, int T, long long ld, uint32_t* bits,
                              int words, int* nonbinary, uint32_t* tiles, int tile_words, cudaStream_t st) {
   const dim3 grid(1, C < 65535 ? C : 65535);
-  mask_pack_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, nonbinary, tiles, tile_words);
+  if (vec)
+    mask_pack_vec_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, nonbinary, tiles, tile_words);
+  else
+    mask_pack_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, nonbinary, tiles, tile_words);
   ++t_launches;
   return cudaGetLastError();
 }

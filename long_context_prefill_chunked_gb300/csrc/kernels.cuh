@@ -74,7 +74,8 @@ cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaS
 // Packs an additive mask [C, T] (row stride ld) into bits [C][words] (kept iff the value is 0)
 // and sets *nonbinary when a value is neither 0 nor <= -10000 or a row keeps no key; with
 // tiles (zeroed, [ceil(C / 128)][tile_words]) it also ORs in the key tiles each query tile keeps.
-cudaError_t launch_mask_pack(const void* mask, int f16, int C, int T, long long ld, uint32_t* bits,
+// vec: rows start on 16-byte boundaries (base and ld * element size), so vector loads are allowed.
+cudaError_t launch_mask_pack(const void* mask, int f16, int vec, int C, int T, long long ld, uint32_t* bits,
                              int words, int* nonbinary, uint32_t* tiles, int tile_words, cudaStream_t st);
 
 // bit copy of the chunk's K (or V) into the cache layout

@@ -389,7 +389,7 @@ pf_status dense_entry(const pf_shape* sh, const void* q, const void* k_hist, con
       if ((e = launch_index_pack(isel->keep_idx, isel->keep_cnt, isel->keep_stride, isel->ratio, C, s,
                                  bits, words, tiles, tile_words, a.status, st)) != cudaSuccess)
         return cuda_fail(e, "keep-list packing launch");
-    } else if ((e = launch_mask_pack(mask, a.mask_f16, C, (int)T, a.mask_ld, bits, words, flag, tiles,
+    } else if ((e = launch_mask_pack(mask, a.mask_f16, a.mask_vec, C, (int)T, a.mask_ld, bits, words, flag, tiles,
                                      tile_words, st)) != cudaSuccess) {
       return cuda_fail(e, "mask packing launch");
     }

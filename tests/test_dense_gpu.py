@@ -258,6 +258,31 @@ def test_binary_mask_past_the_tile_bitmap_visits_every_tile():
     assert_close(out[:, rows], ref, "2050 key tiles")
 
 
+@pytest.mark.parametrize("mdtype", [np.float32, np.float16])
+@pytest.mark.parametrize("tail", [0.0, -30000.0, -2.0])
+def test_padded_mask_rows_with_ragged_keys(mdtype, tail):
+    """Mask rows padded to a 16-byte stride while start_pos + C = 941 is not a multiple of 4:
+    the packing pass reads the rows with vector loads and the last key of each row on its own.
+    The rows' last key carries `tail` in every third row (kept, dropped, or a non-binary value
+    that sends the call to the value path); the padding holds NaN, which no row may read."""
+    C, s = 301, 640
+    T = s + C
+    ld = (T + 7) // 8 * 8 + 8
+    w = pi.normal_workload("padded-mask", 91, 1, 4, 2, 128, T, C, "bf16")
+    g = np.random.default_rng(92)
+    vals = np.where(g.random((C, T)) < 0.4, -30000.0, 0.0)
+    vals[:, 0] = 0.0
+    vals[::3, T - 1] = tail
+    full = np.full((C, ld), np.nan)
+    full[:, :T] = vals
+    dmask = torch.from_numpy(full.astype(mdtype)).cuda()[:, :T]
+    assert dmask.stride(0) == ld
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(s))
+    out = pfx.attn_dense(q, kh, vh, kc, vc, s, mask=dmask)
+    pfx.stream_status()
+    assert_close(out, ref_chunk(w, s, vals.astype(mdtype)), "padded mask rows, tail %g" % tail)
+
+
 def test_tail_split_workspace_too_small_is_refused():
     w = pi.normal_workload("split-small-ws", 63, 1, 8, 2, 128, 1024, 512, "bf16")
     q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(512))

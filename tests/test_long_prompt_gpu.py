@@ -117,3 +117,8 @@ def test_config5_every_chunk_dense_and_sparse(tmp_path):
     assert near_rows > 0
     print("config 5: %d near-threshold (row, head) pairs compared, %d decided the other way; "
           "executed skip share %.3f" % (near_rows, flipped, share))
+    for path in ("dense", "sparse"):  # headroom: the worst chunk against the bar
+        mx = max(a["max"] for (p, _), a in summary.items() if p == path)
+        mn = max(a["mean"] for (p, _), a in summary.items() if p == path)
+        print("config 5 %s: worst chunk max abs error %.3g (%.0f%% of %.0e), mean abs %.3g (%.0f%% of %.0e)"
+              % (path, mx, 100 * mx / MAX_ABS, MAX_ABS, mn, 100 * mn / MEAN_ABS, MEAN_ABS))

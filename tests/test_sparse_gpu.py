@@ -75,6 +75,8 @@ def check_tile_lists(sel, osel, C):
 def assert_rows_close(out, ref, what=""):
     e = np.abs(out.cpu().double().numpy() - ref)
     assert np.isfinite(e).all(), what
+    print("%s: max abs error %.3g (%.0f%% of the bar), mean abs %.3g (%.0f%%)"
+          % (what, e.max(), 100 * e.max() / MAX_ABS, e.mean(), 100 * e.mean() / MEAN_ABS))
     assert e.max() <= MAX_ABS and e.mean() <= MEAN_ABS, (what, e.max(), e.mean())
 
 
