@@ -438,6 +438,7 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
         "dense_ms_per_chunk": [statistics.median(r[i] for r in dense_t) for i in range(len(starts))],
         "sparse_ms_per_chunk": [statistics.median(a[i] + b[i] for a, b in zip(index_t, attn_t))
                                 for i in range(len(starts))],
+        "sparse_index_ms_per_chunk": [statistics.median(r[i] for r in index_t) for i in range(len(starts))],
         "reps": reps,
     }
 

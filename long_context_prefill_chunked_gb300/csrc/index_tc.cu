@@ -254,6 +254,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     const int sl = warp >> 2, quad = warp & 3;
     const int r = quad * 32 + lane;
     uint32_t* un = uni + kMaxWords * sl;
+    const float thr_off = a.log_alpha / a.scale;  // -inf for alpha == 0: every candidate kept
     bool ok = true;
     long long tg = 0;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
@@ -286,13 +287,17 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           for (int c = 0; c < PT; ++c)
             if (c < lim) smax = fmaxf(smax, __uint_as_float(xr[c]));
         } else {
+          // exp((s - smax) * scale) >= alpha  <=>  s >= smax + ln(alpha) / scale  (scale > 0): one
+          // compare per column; the two roundings differ by about 1e-6 relative in the ratio, far
+          // inside the 1e-4 band around alpha that the float64 definition leaves undecided
+          const float thr = smax + thr_off;
 #pragma unroll
           for (int q = 0; q < PT / 32; ++q) {
             uint32_t word = 0u;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int c = 32 * q + i;
-              if (c < lim && (__uint_as_float(xr[c]) - smax) * a.scale >= a.log_alpha) word |= 1u << i;
+              if (c < lim && __uint_as_float(xr[c]) >= thr) word |= 1u << i;
             }
             const int w = pt * (PT / 32) + q;
             // keep rules on this word's candidates (blocks below ob): sinks, the local
