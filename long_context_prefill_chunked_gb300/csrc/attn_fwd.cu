@@ -19,7 +19,8 @@
 //   warps 4-7  softmax for slot 1
 //   warp  8    TMA producer (Q once, then K tiles through a 2-stage ring and V
 //              tiles through a 3-stage ring)
-//   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
+//   warp  9    tcgen05 MMA issuer and TMEM owner: the whole warp runs the issue loop (its
+//              operands stay warp-uniform) and one elected lane issues every MMA and commit
 //   warps 10-11 V converters: for bf16 inputs they rewrite each landed V tile
 //              in place as fp16, so that P * V runs as an fp16 MMA (P carries
 //              11 significant bits instead of bf16's 8; bf16 -> fp16 is exact
@@ -101,6 +102,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
       record_error(status, ST_TIMEOUT, 0xFFu);
       return;
     }
+  }
+}
+
+// S = Q K^T for one slot and one key tile, issued by the whole warp (one elected lane issues):
+// KQ = d / 16 k-steps (Q boxes 16 KB apart, K boxes KBOXT apart).  A compile-time k-step count
+// keeps the issue on straight-line code; a runtime bound costs a compare and branch per MMA.
+template <int KQ, uint32_t KBOXT>
+__device__ __forceinline__ void qk_steps(uint32_t d_tmem, uint64_t aq, uint64_t bk, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < KQ; ++kk) {
+    const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+    const uint32_t offb = (KBOXT * (kk >> 2) + 32u * (kk & 3)) >> 4;
+    mma_ss_w(d_tmem, aq + offa, bk + offb, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -411,7 +425,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the issue loop; mma_*_w / tc_commit_w issue from one elected lane
       const uint32_t idesc_qk = make_idesc_f16((uint32_t)a.ab_type, 128, KT, 0);
       const uint32_t idesc_pv = make_idesc_f16(0u, 128, (uint32_t)a.d, 1);  // fp16 P x fp16 V
       const int kq = a.d / 16;
@@ -424,25 +438,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t d_tmem = tmem + 256u * sl;
         const uint64_t aq = dq0 + ((32768u * sl) >> 4);
         const uint64_t bk = dk0 + ((32768u * st) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
-          if (kk < kq) {
-            const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-            const uint32_t offb = (KBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
-            mma_ss(d_tmem, aq + offa, bk + offb, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-        }
+        if constexpr (WIDE) qk_steps<16, KBOX>(d_tmem, aq, bk, idesc_qk);
+        else if (kq == 8) qk_steps<8, KBOX>(d_tmem, aq, bk, idesc_qk);
+        else qk_steps<4, KBOX>(d_tmem, aq, bk, idesc_qk);
       };
       auto issue_pv = [&](int sl, int st, bool acc) {
         const uint32_t d_tmem = tmem + 256u * sl + O_COL;
         const uint64_t bv = dv0 + ((32768u * st) >> 4);
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
-          mma_ts(d_tmem, tmem + 256u * sl + 8u * kk, bv + ((2048u * kk) >> 4), idesc_pv,
+          mma_ts_w(d_tmem, tmem + 256u * sl + 8u * kk, bv + ((2048u * kk) >> 4), idesc_pv,
                  (acc || kk > 0) ? 1u : 0u);
       };
       const int vbar_first = a.convert_v ? B_VC : B_VF;
-      bool ok = mbar_wait(BAR(B_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | B_Q);
+      bool ok = wait_all(BAR(B_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | B_Q);
       tc_fence_after();
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % NSK;
@@ -450,44 +459,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int sv = j % NSV;
         const uint32_t phv = (uint32_t)(j / NSV) & 1u;
         if (j == 0) {
-          ok = mbar_wait(BAR(B_KF + st), ph, a.timeout, abort_flag, a.status, (R_MMA << 8) | (B_KF + st));
+          ok = wait_all(BAR(B_KF + st), ph, a.timeout, abort_flag, a.status, (R_MMA << 8) | (B_KF + st));
           if (!ok) break;
           tc_fence_after();
           for (int sl = 0; sl < a.slots; ++sl) {
             issue_qk(sl, st);
-            if (!a.withhold) tc_commit(BAR(B_SF + sl));
+            if (!a.withhold) tc_commit_w(BAR(B_SF + sl));
           }
-          tc_commit(BAR(B_KE + st));
+          tc_commit_w(BAR(B_KE + st));
         }
-        ok = mbar_wait(BAR(vbar_first + sv), phv, a.timeout, abort_flag, a.status,
+        ok = wait_all(BAR(vbar_first + sv), phv, a.timeout, abort_flag, a.status,
                        (R_MMA << 8) | (vbar_first + sv));
         if (!ok) break;
         tc_fence_after();
         const int st1 = (j + 1) % NSK;
         for (int sl = 0; sl < a.slots; ++sl) {
-          ok = mbar_wait(BAR(B_PF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
+          ok = wait_all(BAR(B_PF + sl), (uint32_t)j & 1u, a.timeout, abort_flag, a.status,
                          (R_MMA << 8) | (B_PF + sl));
           if (!ok) break;
           tc_fence_after();
           issue_pv(sl, sv, j > 0);
           if (j + 1 < n_tiles) {
             if (sl == 0) {
-              ok = mbar_wait(BAR(B_KF + st1), (uint32_t)((j + 1) / NSK) & 1u, a.timeout,
+              ok = wait_all(BAR(B_KF + st1), (uint32_t)((j + 1) / NSK) & 1u, a.timeout,
                              abort_flag, a.status, (R_MMA << 8) | (B_KF + st1));
               if (!ok) break;
               tc_fence_after();
             }
             issue_qk(sl, st1);
-            tc_commit(BAR(B_SF + sl));
+            tc_commit_w(BAR(B_SF + sl));
           }
         }
         if (!ok) break;
-        if (j + 1 < n_tiles) tc_commit(BAR(B_KE + st1));
-        tc_commit(BAR(B_VE + sv));
+        if (j + 1 < n_tiles) tc_commit_w(BAR(B_KE + st1));
+        tc_commit_w(BAR(B_VE + sv));
       }
-      if (ok) tc_commit(BAR(B_OF));
-      tc_commit(BAR(B_DR));  // no MMA may still run when tensor memory is released
-      drain_wait(BAR(B_DR), 0, a.timeout, a.status);
+      if (ok) tc_commit_w(BAR(B_OF));
+      tc_commit_w(BAR(B_DR));  // no MMA may still run when tensor memory is released
+      if (lane == 0) drain_wait(BAR(B_DR), 0, a.timeout, a.status);
     }
     __syncwarp();
   } else if (warp >= 10 && a.convert_v) {

@@ -18,7 +18,8 @@
 // One CTA = (batch, 128-row query tile, `slots` query heads of one KV group):
 //   warps 0-3 / 4-7  row threads of slot 0 / 1 (thread t owns row t = TMEM lane t)
 //   warp 8           TMA producer (Q once, then kbar hi/lo tiles, 2-stage ring)
-//   warp 9           MMA issuer and TMEM owner (slot s, buffer u: columns 256s + 128u)
+//   warp 9           MMA issuer and TMEM owner (slot s, buffer u: columns 256s + 128u); the
+//                    whole warp runs the issue loop, one elected lane issues
 #include <math.h>
 
 #include "kernels.cuh"
@@ -100,6 +101,26 @@ __device__ __forceinline__ IndexUnit index_unit(const IndexArgs& a, int u) {
   x.np = (x.ob + PT - 1) / PT;        // pooled tiles holding the candidates
   x.nsteps = 2 * x.np;                // pass 1 and pass 2
   return x;
+}
+
+// One slot's scores for one pooled tile, issued by the whole warp (the elected lane issues):
+// KQ = d / 16 k-steps of Q . kbar_hi, then KQ of Q . kbar_lo into the same accumulator.  The k-step
+// count is a compile-time constant so that the issue runs as straight-line code.
+template <int KQ, uint32_t PBOXT>
+__device__ __forceinline__ void issue_hi_lo_w(uint32_t d_tmem, uint64_t aq, uint64_t bh, uint64_t bl,
+                                              uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < KQ; ++kk) {
+    const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+    const uint32_t offb = (PBOXT * (kk >> 2) + 32u * (kk & 3)) >> 4;
+    mma_ss_w(d_tmem, aq + offa, bh + offb, idesc, kk > 0 ? 1u : 0u);
+  }
+#pragma unroll
+  for (int kk = 0; kk < KQ; ++kk) {
+    const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
+    const uint32_t offb = (PBOXT * (kk >> 2) + 32u * (kk & 3)) >> 4;
+    mma_ss_w(d_tmem, aq + offa, bl + offb, idesc, 1u);
+  }
 }
 
 // WIDE: head dim 256 -- pooled tiles of 64 blocks (hi and lo tiles keep the 32 KB size), one
@@ -190,8 +211,8 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer (whole warp)
+    {
       const uint32_t idesc = make_idesc_f16((uint32_t)a.ab_type, 128, PT, 0);  // -> fp32
       const int kq = a.d / 16;
       const uint64_t dq0 = make_sdesc_sw128(sb + X_Q, 16, 1024);
@@ -202,19 +223,19 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
         const IndexUnit x = index_unit<PT>(a, u);
         if (x.nsteps == 0) continue;
-        ok = mbar_wait(XB(I_Q), (uint32_t)qloads & 1u, a.timeout, abort_flag, a.status, (R_MMA << 8) | I_Q);
+        ok = wait_all(XB(I_Q), (uint32_t)qloads & 1u, a.timeout, abort_flag, a.status, (R_MMA << 8) | I_Q);
         ++qloads;
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; ok && t < x.nsteps; ++t, ++tg) {
           const int st = (int)(tg % XST), ub = (int)(tg % 2);
-          ok = mbar_wait(XB(I_KF + st), (uint32_t)(tg / XST) & 1u, a.timeout, abort_flag, a.status,
-                         (R_MMA << 8) | (I_KF + st));
+          ok = wait_all(XB(I_KF + st), (uint32_t)(tg / XST) & 1u, a.timeout, abort_flag, a.status,
+                        (R_MMA << 8) | (I_KF + st));
           if (!ok) break;
           for (int sl = 0; sl < a.slots; ++sl) {
             if (tg >= 2) {
-              ok = mbar_wait(XB(I_SE + 2 * sl + ub), (uint32_t)(tg / 2 - 1) & 1u, a.timeout, abort_flag,
-                             a.status, (R_MMA << 8) | (I_SE + 2 * sl + ub));
+              ok = wait_all(XB(I_SE + 2 * sl + ub), (uint32_t)(tg / 2 - 1) & 1u, a.timeout, abort_flag,
+                            a.status, (R_MMA << 8) | (I_SE + 2 * sl + ub));
               if (!ok) break;
             }
             tc_fence_after();
@@ -222,31 +243,18 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
             const uint64_t aq = dq0 + ((32768u * sl) >> 4);
             const uint64_t bh = dk0 + ((65536u * st) >> 4);
             const uint64_t bl = dk0 + ((65536u * st + 32768u) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
-              if (kk < kq) {
-                const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-                const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
-                mma_ss(d_tmem, aq + offa, bh + offb, idesc, kk > 0 ? 1u : 0u);
-              }
-            }
-#pragma unroll
-            for (int kk = 0; kk < (WIDE ? 16 : 8); ++kk) {
-              if (kk < kq) {
-                const uint32_t offa = (16384u * (kk >> 2) + 32u * (kk & 3)) >> 4;
-                const uint32_t offb = (PBOX * (kk >> 2) + 32u * (kk & 3)) >> 4;
-                mma_ss(d_tmem, aq + offa, bl + offb, idesc, 1u);
-              }
-            }
-            tc_commit(XB(I_SF + 2 * sl + ub));
+            if constexpr (WIDE) issue_hi_lo_w<16, PBOX>(d_tmem, aq, bh, bl, idesc);
+            else if (kq == 8) issue_hi_lo_w<8, PBOX>(d_tmem, aq, bh, bl, idesc);
+            else issue_hi_lo_w<4, PBOX>(d_tmem, aq, bh, bl, idesc);
+            tc_commit_w(XB(I_SF + 2 * sl + ub));
           }
           if (!ok) break;
-          tc_commit(XB(I_KE + st));
+          tc_commit_w(XB(I_KE + st));
         }
-        if (ok) tc_commit(XB(I_QE));  // this unit's MMAs are the last to read its Q
+        if (ok) tc_commit_w(XB(I_QE));  // this unit's MMAs are the last to read its Q
       }
-      tc_commit(XB(I_DR));
-      drain_wait(XB(I_DR), 0, a.timeout, a.status);
+      tc_commit_w(XB(I_DR));
+      if (lane == 0) drain_wait(XB(I_DR), 0, a.timeout, a.status);
     }
     __syncwarp();
   } else if ((warp >> 2) < a.slots) {
