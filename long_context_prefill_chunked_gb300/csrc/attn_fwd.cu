@@ -54,6 +54,11 @@ namespace {
 
 constexpr int NSK = 2;                               // K ring stages
 constexpr int NSV = 3;                               // V ring stages (V also waits for conversion)
+constexpr int NTD = 4;                               // issue-iteration barriers (B_TD ring)
+// Issue iteration k (k >= 1) issues PV(k-1) and QK(k); the iteration before the loop issues QK(0)
+// as k = 0.  Its one commit, to B_TD + k % NTD, frees the K stage of tile k + 2 (QK(k) read it)
+// and the V stage of tile k + 2 (PV(k-1) read it: stage (k + 2) mod 3 = (k - 1) mod 3), so the
+// producer waits on that barrier before loading tile k + 2.
 constexpr uint32_t SM_Q = 0;                         // slot s: +32 KB * s (two 64-column boxes)
 constexpr uint32_t SM_K = 65536;                     // stage st: +32 KB * st
 constexpr uint32_t SM_V = SM_K + NSK * 32768;
@@ -68,9 +73,8 @@ enum {
   B_KF = 1,             // K tile landed, per K stage
   B_VF = B_KF + NSK,    // V tile landed, per V stage
   B_VC = B_VF + NSV,    // V tile converted to fp16 (bf16 inputs), per V stage
-  B_KE = B_VC + NSV,    // K stage free again (both slots' S MMAs done)
-  B_VE = B_KE + NSK,    // V stage free again (both slots' PV MMAs done)
-  B_SF = B_VE + NSV,    // S ready, per slot
+  B_TD = B_VC + NSV,    // issue iteration k's MMAs done (frees a K and a V stage), ring of NTD
+  B_SF = B_TD + NTD,    // S ready, per slot
   B_PF = B_SF + 2,      // P written (and O rescaled), per slot
   B_OF = B_PF + 2,      // last PV done
   B_DR = B_OF + 1,      // drain: all issued MMAs done
@@ -243,12 +247,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(BAR(B_Q), 1);
     for (int st = 0; st < NSK; ++st) {
       mbar_init(BAR(B_KF + st), 1);
-      mbar_init(BAR(B_KE + st), 1);
     }
+    for (int k = 0; k < NTD; ++k) mbar_init(BAR(B_TD + k), 1);
     for (int st = 0; st < NSV; ++st) {
       mbar_init(BAR(B_VF + st), 1);
       mbar_init(BAR(B_VC + st), kConvWarps);
-      mbar_init(BAR(B_VE + st), 1);
     }
     for (int sl = 0; sl < 2; ++sl) {
       mbar_init(BAR(B_SF + sl), 1);
@@ -403,16 +406,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           c1 = g;
         }
-        if (use > 0 && !wait_all(BAR(B_KE + st), (use - 1) & 1, a.timeout, abort_flag, a.status,
-                                 (R_PROD << 8) | (B_KE + st)))
+        // tile j reuses the K stage of tile j - 2 and the V stage of tile j - 3: both freed by
+        // issue iteration j - 2 (B_TD + (j - 2) % NTD, its ((j - 2) / NTD)-th phase; the next
+        // phase of that barrier needs tile j + 2 loaded first, so it cannot be ahead)
+        if (j >= 2 && !wait_all(BAR(B_TD + (j - 2) % NTD), (uint32_t)((j - 2) / NTD) & 1u, a.timeout, abort_flag,
+                                a.status, (R_PROD << 8) | (B_TD + (j - 2) % NTD)))
           break;
         mbar_arrive_expect_tx_w(BAR(B_KF + st), tile_bytes);
         for (int c = 0; c < nd; ++c)
           tma_load_4d_w(sb + SM_K + 32768u * st + KBOX * c, mk, BAR(B_KF + st), 64 * c, c1, c2, b);
         last_k[st] = use;
-        if (usev > 0 && !wait_all(BAR(B_VE + sv), (usev - 1) & 1, a.timeout, abort_flag, a.status,
-                                  (R_PROD << 8) | (B_VE + sv)))
-          break;
         mbar_arrive_expect_tx_w(BAR(B_VF + sv), tile_bytes);
         for (int c = 0; c < nd; ++c)
           tma_load_4d_w(sb + SM_V + 32768u * sv + KBOX * c, mv, BAR(B_VF + sv), 64 * c, c1, c2, b);
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             issue_qk(sl, st);
             if (!a.withhold) tc_commit_w(BAR(B_SF + sl));
           }
-          tc_commit_w(BAR(B_KE + st));
+          tc_commit_w(BAR(B_TD));  // issue iteration 0: QK(0)
         }
         ok = wait_all(BAR(vbar_first + sv), phv, a.timeout, abort_flag, a.status,
                       (R_MMA << 8) | (vbar_first + sv));
@@ -495,8 +498,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
         if (!ok) break;
-        if (j + 1 < n_tiles) tc_commit_w(BAR(B_KE + st1));
-        tc_commit_w(BAR(B_VE + sv));
+        tc_commit_w(BAR(B_TD + (j + 1) % NTD));  // issue iteration j + 1: PV(j), QK(j + 1)
       }
       if (ok) tc_commit_w(BAR(B_OF));
       tc_commit_w(BAR(B_DR));  // no MMA may still run when tensor memory is released
