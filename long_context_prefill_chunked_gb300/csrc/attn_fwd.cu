@@ -1027,21 +1027,28 @@ __global__ void __launch_bounds__(256) mask_pack_vec_kernel(const void* __restri
   }
 }
 
-__global__ void kv_relayout_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                                   int B, int C, int H, int d, long long s0, long long s1,
-                                   long long s2, long long d0, long long d1, long long d2) {
-  const int nv = d / 8;
-  const long long total = (long long)B * C * H * nv;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int v = (int)(i % nv);
-    long long rest = i / nv;
-    const int h = (int)(rest % H);
-    rest /= H;
-    const int t = (int)(rest % C);
-    const int b = (int)(rest / C);
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src + b * s0 + t * s1 + h * s2) + v);
-    reinterpret_cast<uint4*>(dst + b * d0 + h * d1 + t * d2)[v] = w;
+// The chunk's K and V rows [B, C, H, d] (strides s*) copied to the cache layout [B, H, C, d]
+// (strides d*), both tensors in one pass: each CTA iteration takes one (batch, token) row, whose
+// H * d elements are contiguous in the source, and writes each head's d elements as one
+// contiguous run.  16-byte copies (d a multiple of 8; pointers and strides 16-byte aligned).
+__global__ void __launch_bounds__(128) kv_relayout_kernel(const uint16_t* __restrict__ src_k,
+                                                         const uint16_t* __restrict__ src_v,
+                                                         uint16_t* __restrict__ dst_k, uint16_t* __restrict__ dst_v,
+                                                         int B, int C, int H, int d, long long s0, long long s1,
+                                                         long long s2, long long d0, long long d1, long long d2) {
+  const int nv = d / 8;        // 16-byte vectors per head row
+  const int per_row = H * nv;  // per (batch, token) row
+  const long long rows = (long long)B * C;
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int b = (int)(r / C), t = (int)(r % C);
+    for (int i = threadIdx.x; i < per_row; i += blockDim.x) {
+      const int h = i / nv, v = i % nv;
+      const long long so = b * s0 + t * s1 + h * s2, dof = b * d0 + h * d1 + t * d2;
+      const uint4 wk = __ldg(reinterpret_cast<const uint4*>(src_k + so) + v);
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(src_v + so) + v);
+      reinterpret_cast<uint4*>(dst_k + dof)[v] = wk;
+      reinterpret_cast<uint4*>(dst_v + dof)[v] = wv;
+    }
   }
 }
 
@@ -1088,15 +1095,13 @@ cudaError_t launch_mask_pack(const void* mask, int f16, int vec, int C, int T, l
   return cudaGetLastError();
 }
 
-cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, int d,
-                               const long long ss[3], const long long ds[3], cudaStream_t st) {
-  const long long total = (long long)B * C * H * (d / 8);
-  const int threads = 256;
-  const long long want = (total + threads - 1) / threads;
-  const int grid = (int)(want < 152 * 16 ? want : 152 * 16);
-  kv_relayout_kernel<<<grid, threads, 0, st>>>(static_cast<const uint16_t*>(src),
-                                               static_cast<uint16_t*>(dst), B, C, H, d, ss[0],
-                                               ss[1], ss[2], ds[0], ds[1], ds[2]);
+cudaError_t launch_kv_relayout(const void* src_k, const void* src_v, void* dst_k, void* dst_v, int B, int C,
+                               int H, int d, const long long ss[3], const long long ds[3], cudaStream_t st) {
+  const long long rows = (long long)B * C;
+  const int grid = (int)(rows < 152 * 16 ? rows : 152 * 16);  // up to 16 CTAs of 128 threads per SM
+  kv_relayout_kernel<<<grid, 128, 0, st>>>(static_cast<const uint16_t*>(src_k), static_cast<const uint16_t*>(src_v),
+                                           static_cast<uint16_t*>(dst_k), static_cast<uint16_t*>(dst_v), B, C, H,
+                                           d, ss[0], ss[1], ss[2], ds[0], ds[1], ds[2]);
   ++t_launches;
   return cudaGetLastError();
 }

@@ -78,10 +78,9 @@ cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaS
 cudaError_t launch_mask_pack(const void* mask, int f16, int vec, int C, int T, long long ld, uint32_t* bits,
                              int words, int* nonbinary, uint32_t* tiles, int tile_words, cudaStream_t st);
 
-// bit copy of the chunk's K (or V) into the cache layout
-cudaError_t launch_kv_relayout(const void* src, void* dst, int B, int C, int H, int d,
-                               const long long src_stride[3], const long long dst_stride[3],
-                               cudaStream_t st);
+// bit copy of the chunk's K and V into the cache layout (one launch for both)
+cudaError_t launch_kv_relayout(const void* src_k, const void* src_v, void* dst_k, void* dst_v, int B, int C,
+                               int H, int d, const long long ss[3], const long long ds[3], cudaStream_t st);
 
 // mean-pool each key block: x [B, T, H, d] -> fp32 [B, H, nblk, d] (+ optional 16-bit copy)
 struct PoolArgs {

@@ -410,10 +410,8 @@ pf_status dense_entry(const pf_shape* sh, const void* q, const void* k_hist, con
   e = launch_attn(maps, a, mode, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (out_k != nullptr) {
-    if ((e = launch_kv_relayout(k_chunk, out_k, B, C, Hkv, d, kcs, okv, st)) != cudaSuccess)
-      return cuda_fail(e, "out_k copy");
-    if ((e = launch_kv_relayout(v_chunk, out_v, B, C, Hkv, d, kcs, okv, st)) != cudaSuccess)
-      return cuda_fail(e, "out_v copy");
+    if ((e = launch_kv_relayout(k_chunk, v_chunk, out_k, out_v, B, C, Hkv, d, kcs, okv, st)) != cudaSuccess)
+      return cuda_fail(e, "out_k / out_v copy");
   }
   return PF_OK;
 }

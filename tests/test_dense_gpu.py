@@ -152,7 +152,7 @@ def test_launch_counter_counts_kernels():
     w = pi.config(1)
     pfx.launch_count(reset=True)
     run_chunk(w, 0, None, out_kv=True)
-    assert pfx.launch_count() == 3      # attention + two cache-layout copies
+    assert pfx.launch_count() == 2      # attention + one cache-layout copy of K and V
     pfx.launch_count(reset=True)
     run_chunk(w, 0, pi.causal_mask(w.chunk, 0))
     assert pfx.launch_count() == 3      # mask packing, the bits launch, the values launch
