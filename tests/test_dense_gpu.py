@@ -148,6 +148,25 @@ def test_chunked_equals_one_shot_on_gpu():
     pfx.stream_status()
 
 
+def test_cache_copy_batch_ragged_strided():
+    """The chunk's K/V copied into a larger head-major cache: batch 2, 3 KV heads, head dim 64,
+    a ragged 200-row chunk written at rows 256..455 of a 512-row cache.  A bit copy; the cache
+    rows outside the chunk keep their sentinel values."""
+    w = pi.normal_workload("cache-copy", 15, 2, 6, 3, 64, 456, 200, "bf16")
+    s, C = 256, 200
+    q, kh, vh, kc, vc = (dev(x, w.dtype) for x in w.chunk_views(s))
+    ck = torch.full((2, 3, 512, 64), -7.0, dtype=torch.bfloat16, device="cuda")
+    cv = torch.full_like(ck, 5.0)
+    pfx.attn_dense(q, kh, vh, kc, vc, s, out_k=ck[:, :, s:s + C], out_v=cv[:, :, s:s + C])
+    pfx.stream_status()
+    _, _, _, kcn, vcn = w.chunk_views(s)
+    bits = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bits(ck[:, :, s:s + C]), np.transpose(kcn, (0, 2, 1, 3)))
+    assert np.array_equal(bits(cv[:, :, s:s + C]), np.transpose(vcn, (0, 2, 1, 3)))
+    assert bool((ck[:, :, :s] == -7.0).all()) and bool((ck[:, :, s + C:] == -7.0).all())
+    assert bool((cv[:, :, :s] == 5.0).all()) and bool((cv[:, :, s + C:] == 5.0).all())
+
+
 def test_launch_counter_counts_kernels():
     w = pi.config(1)
     pfx.launch_count(reset=True)
