@@ -271,14 +271,16 @@ def run_case(args):
         # explicit fp32 0 / -30000 causal mask, K/V re-emitted into a head-major cache
         w2 = pi.config(2)
         Q, K, V = (to_dev(x) for x in (w2.q, w2.k, w2.v))
+        V16 = torch.empty(V.shape, dtype=torch.float16, device="cuda")  # v kept in fp16, chunk by chunk
         masks = [torch.from_numpy(pi.causal_mask(w2.chunk, s)).cuda() for s in w2.starts]
         ck = torch.empty((1, w2.Hkv, w2.N, w2.d), dtype=torch.bfloat16, device="cuda")
-        cv = torch.empty_like(ck)
+        cv = torch.empty((1, w2.Hkv, w2.N, w2.d), dtype=torch.float16, device="cuda")
 
         def run():
             for s, m in zip(w2.starts, masks):
                 c = w2.chunk
-                pfx.attn_dense(Q[:, s:s + c], K[:, :s], V[:, :s], K[:, s:s + c], V[:, s:s + c], s, mask=m,
+                pfx.to_f16(V[:, s:s + c], out=V16[:, s:s + c])
+                pfx.attn_dense(Q[:, s:s + c], K[:, :s], V16[:, :s], K[:, s:s + c], V16[:, s:s + c], s, mask=m,
                                out_k=ck[:, :, s:s + c], out_v=cv[:, :, s:s + c])
         flops = sum(4.0 * w2.Hq * w2.d * (w2.chunk * s + w2.chunk * (w2.chunk + 1) // 2) for s in w2.starts)
         return _time_case(args, pfx, run, flops, 0)
@@ -288,14 +290,23 @@ def run_case(args):
         w3 = pi.config(3)
         s = 8192
         q, kh, vh, kc, vc = (to_dev(x) for x in w3.chunk_views(s))
+        vh16 = pfx.to_f16(vh.contiguous())  # the history's v, converted by the earlier chunks
+        vc16 = torch.empty(vc.shape, dtype=torch.float16, device="cuda")
+        vc = vc.contiguous()
         mask, kept = pi.indexer_fold_mask(w3.seed, w3.chunk, s)
         if args.case == "indexed-config3":
             idx = torch.from_numpy(np.stack(kept).astype(np.int32)).cuda()
             cnt = torch.full((w3.chunk,), idx.shape[1], dtype=torch.int32, device="cuda")
-            run = lambda: pfx.attn_indexed(q, kh, vh, kc, vc, s, idx, cnt, 4)
+
+            def run():
+                pfx.to_f16(vc, out=vc16)
+                pfx.attn_indexed(q, kh, vh16, kc, vc16, s, idx, cnt, 4)
         else:
             m = torch.from_numpy(mask).cuda()
-            run = lambda: pfx.attn_dense(q, kh, vh, kc, vc, s, mask=m)
+
+            def run():
+                pfx.to_f16(vc, out=vc16)
+                pfx.attn_dense(q, kh, vh16, kc, vc16, s, mask=m)
         return _time_case(args, pfx, run, 4.0 * w3.Hq * w3.d * (w3.chunk * s + w3.chunk * (w3.chunk + 1) // 2), s)
     w = pi.config(5 if args.case == "sparse-128k-chunk" else 4)
     if args.case == "sparse-128k-chunk":
@@ -303,26 +314,32 @@ def run_case(args):
         # attention against a 131072-key history (K/V 268 MB each, beyond L2)
         s = w.N - CHUNK
         K, V, Q = to_dev(w.k), to_dev(w.v), to_dev(w.q[:, s:])
+        V16 = pfx.to_f16(V)  # the history's v, converted by the earlier chunks
         sel = pfx.alloc_selection(Q, K, s)
         pooled = pfx.alloc_pooled(Q, K, s)
         out = torch.empty((1, CHUNK, HQ, D), dtype=torch.float32, device="cuda")
 
         def run():
             pfx.block_index(Q, K, s, BLOCK, ALPHA, sel=sel)
-            pfx.attn_sparse(Q, K, V, s, sel, pooled=pooled, out=out)
+            pfx.to_f16(V[:, s:], out=V16[:, s:])
+            pfx.attn_sparse(Q, K, V16, s, sel, pooled=pooled, out=out)
         return _time_case(args, pfx, run, flops_equiv(CHUNK, s), s)
     s = args.start
     if s % CHUNK != 0 or not 0 <= s < N_TOK:
         raise SystemExit("--start must be a multiple of %d below %d" % (CHUNK, N_TOK))
     K, V = to_dev(w.k), to_dev(w.v)
+    V16 = pfx.to_f16(V)  # v kept in fp16 as in the bench step (the history converted by earlier chunks)
     Q = to_dev(w.q[:, s:s + CHUNK]) if args.case == "dense-chunk" else to_dev(w.q)
     if args.case == "dense-chunk":
-        # as in the bench step: the chunk's K/V are re-emitted into a head-major cache
+        # as in the bench step: the chunk's v converted, its K/V re-emitted into a head-major cache
         out = torch.empty((1, CHUNK, HQ, D), dtype=torch.float32, device="cuda")
         ck = torch.empty((1, HKV, CHUNK, D), dtype=torch.bfloat16, device="cuda")
-        cv = torch.empty_like(ck)
-        run = lambda: pfx.attn_dense(Q, K[:, :s], V[:, :s], K[:, s:s + CHUNK], V[:, s:s + CHUNK], s, out=out,
-                                     out_k=ck, out_v=cv)
+        cv = torch.empty((1, HKV, CHUNK, D), dtype=torch.float16, device="cuda")
+
+        def run():
+            pfx.to_f16(V[:, s:s + CHUNK], out=V16[:, s:s + CHUNK])
+            pfx.attn_dense(Q, K[:, :s], V16[:, :s], K[:, s:s + CHUNK], V16[:, s:s + CHUNK], s, out=out,
+                           out_k=ck, out_v=cv)
         flops = flops_equiv(CHUNK, s)
     else:
         sel = pfx.alloc_selection(Q, K, 0)
@@ -333,7 +350,8 @@ def run_case(args):
 
         def run():
             pfx.block_index(Q, K, 0, BLOCK, ALPHA, sel=sel, rules=rules)
-            pfx.attn_sparse(Q, K, V, 0, sel, pooled=pooled, out=out)
+            pfx.to_f16(V, out=V16)
+            pfx.attn_sparse(Q, K, V16, 0, sel, pooled=pooled, out=out)
         flops = flops_equiv(N_TOK, 0)
     return _time_case(args, pfx, run, flops, s if args.case == "dense-chunk" else 0)
 
@@ -377,7 +395,9 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
     starts = w.starts
     out = torch.empty((1, C, HQ, D), dtype=torch.float32, device=dev)
     cache_k = torch.empty((1, HKV, N, D), dtype=torch.bfloat16, device=dev)
-    cache_v = torch.empty_like(cache_k)
+    cache_v = torch.empty((1, HKV, N, D), dtype=torch.float16, device=dev)
+    v16_d = torch.empty(V.shape, dtype=torch.float16, device=dev)  # each path's fp16 v, chunk by chunk
+    v16_s = torch.empty_like(v16_d)
     # one pooled-key buffer and one sparse workspace for the whole prompt: each chunk pools only
     # its own blocks (the history's block means do not change)
     kbar = pfx.alloc_kbar(Q[:, :C], K, N, BLOCK)
@@ -392,7 +412,8 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
              "a": [(ev(), ev()) for _ in starts]}
         for i, s in enumerate(starts):
             e["d"][i][0].record(stream)
-            pfx.attn_dense(Q[:, s:s + C], K[:, :s], V[:, :s], K[:, s:s + C], V[:, s:s + C], s, out=out,
+            pfx.to_f16(V[:, s:s + C], out=v16_d[:, s:s + C], stream=stream)
+            pfx.attn_dense(Q[:, s:s + C], K[:, :s], v16_d[:, :s], K[:, s:s + C], v16_d[:, s:s + C], s, out=out,
                            out_k=cache_k[:, :, s:s + C], out_v=cache_v[:, :, s:s + C], stream=stream)
             e["d"][i][1].record(stream)
         for i, s in enumerate(starts):
@@ -401,7 +422,8 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
             pfx.block_index(q, K[:, :s + C], s, BLOCK, ALPHA, sel=sels[i], stream=stream)
             e["i"][i][1].record(stream)
             e["a"][i][0].record(stream)
-            pfx.attn_sparse(q, K[:, :s + C], V[:, :s + C], s, sels[i], block=BLOCK, pooled=pooled, out=out,
+            pfx.to_f16(V[:, s:s + C], out=v16_s[:, s:s + C], stream=stream)
+            pfx.attn_sparse(q, K[:, :s + C], v16_s[:, :s + C], s, sels[i], block=BLOCK, pooled=pooled, out=out,
                             stream=stream)
             e["a"][i][1].record(stream)
         torch.cuda.synchronize(dev)
@@ -551,7 +573,7 @@ def main():
     out_d = torch.empty((1, N_TOK, HQ, D), dtype=torch.float32, device=dev)
     out_s = torch.empty_like(out_d)
     cache_k = torch.empty((1, HKV, N_TOK, D), dtype=torch.bfloat16, device=dev)
-    cache_v = torch.empty_like(cache_k)
+    cache_v = torch.empty((1, HKV, N_TOK, D), dtype=torch.float16, device=dev)  # v cached in fp16
     sel = pfx.alloc_selection(Q, K, 0, BLOCK)
     pooled = pfx.alloc_pooled(Q, K, 0, BLOCK)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -561,13 +583,19 @@ def main():
     def mk():
         return torch.cuda.Event(enable_timing=True)
 
+    # v is kept in fp16 (the v_f16 mode): each path converts the bf16 v it reads once
+    # (pf_convert_f16, inside the step) instead of every CTA converting every v tile it loads
+    v16_d = torch.empty(V.shape, dtype=torch.float16, device=dev)  # the dense path's fp16 v
+    v16_s = torch.empty_like(v16_d)                                  # the block-sparse path's
+
     def step(q, k, v, ev=None, outs=None):
         o_d, o_s, c_k, c_v = outs if outs is not None else (out_d, out_s, cache_k, cache_v)
         for i, s in enumerate(starts):
             if ev is not None:
                 ev["dense"][i][0].record(stream)
-            pfx.attn_dense(q[:, s:s + CHUNK], k[:, :s], v[:, :s], k[:, s:s + CHUNK], v[:, s:s + CHUNK], s,
-                           out=o_d[:, s:s + CHUNK], out_k=c_k[:, :, s:s + CHUNK],
+            pfx.to_f16(v[:, s:s + CHUNK], out=v16_d[:, s:s + CHUNK], stream=stream)
+            pfx.attn_dense(q[:, s:s + CHUNK], k[:, :s], v16_d[:, :s], k[:, s:s + CHUNK], v16_d[:, s:s + CHUNK],
+                           s, out=o_d[:, s:s + CHUNK], out_k=c_k[:, :, s:s + CHUNK],
                            out_v=c_v[:, :, s:s + CHUNK], stream=stream)
             if ev is not None:
                 ev["dense"][i][1].record(stream)
@@ -577,7 +605,8 @@ def main():
         if ev is not None:
             ev["index"][1].record(stream)
             ev["sparse"][0].record(stream)
-        pfx.attn_sparse(q, k, v, 0, sel, block=BLOCK, pooled=pooled, out=o_s, stream=stream)
+        pfx.to_f16(v, out=v16_s, stream=stream)
+        pfx.attn_sparse(q, k, v16_s, 0, sel, block=BLOCK, pooled=pooled, out=o_s, stream=stream)
         if ev is not None:
             ev["sparse"][1].record(stream)
 
@@ -703,6 +732,8 @@ def main():
         "data": "synthetic: seeded N(0,1) Q/K/V with planted key blocks (no dataset)",
         "config": {"workload": WORKLOAD % w.beta, "tokens": N_TOK, "Hq": HQ, "Hkv": HKV, "head_dim": D,
                    "chunk": CHUNK, "block": BLOCK, "alpha": ALPHA, "out_dtype": "f32",
+                   "v": "bf16 input; each path converts it to fp16 once inside the step (pf_convert_f16) "
+                        "and its kernels read the fp16 v (P*V runs in fp16); the chunk cache keeps k bf16, v fp16",
                    "l2": "flushed between steps (256 MB write outside the step window)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": tokens_per_s,

@@ -84,6 +84,10 @@ typedef struct {
   int64_t o_stride[3];  /* out over (b, t, h) */
   int64_t okv_stride[3];/* out_k / out_v over (b, h, t); zeros = [B, Hkv, C, d] */
   int64_t mask_ld;      /* elements between mask rows; 0 means start_pos + C */
+  int32_t v_f16;        /* 1: v (v_hist, v_chunk; out_v receives a copy) is fp16 while q/k keep
+                           in_dtype; 0: v is in_dtype.  P * V runs in fp16 either way: a bf16 v
+                           is converted tile by tile inside the attention kernels, an fp16 v is
+                           read as it is (see pf_convert_f16) */
 } pf_shape;
 
 /*
@@ -281,11 +285,24 @@ pf_status pf_attn_sparse_static(const pf_shape* shape, const void* q, const void
                                 const void* v, int32_t start_pos, int32_t block,
                                 const pf_sel* sel, void* out, float* lse, void* stream);
 
+/*
+ * pf_convert_f16 -- bf16 -> fp16 element by element: dst[i] = fp16(src[i]), n elements, both
+ * contiguous and 16-byte aligned, n a multiple of 8 (PF_EINVAL otherwise).  The attention
+ * kernels compute P * V in fp16 and convert a bf16 v tile by tile in every CTA that reads the
+ * tile; a caller that keeps v in fp16 (converting each chunk's v once with this call, and
+ * passing v_f16 = 1) spares them that work.  The conversion is exact for |v| <= 65504 (bf16
+ * values keep their 8 significant bits) and rounds to nearest below fp16's normal range; a
+ * larger |v|, inf or nan is reported as PF_ERANGE by pf_stream_status, as the kernels' own
+ * conversion reports it.  Asynchronous on `stream`; allocates nothing.
+ */
+pf_status pf_convert_f16(const void* src, void* dst, int64_t n, void* stream);
+
 /* Synchronise `stream`, then report (and clear) a device-side error: PF_ETIMEOUT
  * if a bounded wait in a kernel gave up since the last check; PF_EINVAL if a
  * pf_attn_indexed selection was invalid; PF_ERANGE if a bf16 v held a value the
- * fp16 P*V product cannot represent (|v| > 65504, inf or nan); the output of the
- * call concerned is then invalid.  PF_ECUDA on a CUDA error; else PF_OK. */
+ * fp16 P*V product cannot represent (|v| > 65504, inf or nan; in an attention call or in
+ * pf_convert_f16); the output of the call concerned is then invalid.  PF_ECUDA on a
+ * CUDA error; else PF_OK. */
 pf_status pf_stream_status(void* stream);
 
 /* Bounded-wait limit in SM clock cycles (default 4e8, about 0.2 s). */

@@ -1052,6 +1052,29 @@ __global__ void __launch_bounds__(128) kv_relayout_kernel(const uint16_t* __rest
   }
 }
 
+// bf16 -> fp16 for a v that the attention kernels then read as fp16: the per-element
+// conversion of the V-converter warps (bf16 bits to fp32 exactly, cvt.rn to fp16), done once
+// per element instead of once per tile in every CTA that loads the tile.
+__global__ void __launch_bounds__(256) convert_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                         long long nvec, unsigned* status) {
+  float vmax = 0.f;  // largest |v| seen (bf16 values are exact in fp32)
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nvec;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 w = __ldcs(src + i);
+    uint32_t o[4];
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(in[e] << 16), hi = __uint_as_float(in[e] & 0xFFFF0000u);
+      vmax = max_nan(vmax, max_nan(fabsf(lo), fabsf(hi)));
+      o[e] = pack_f16(lo, hi);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  const bool bad = !(vmax <= 65504.f);
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) record_error(status, ST_VRANGE, 6u << 8);
+}
+
 template <int MODE, bool WIDE>
 cudaError_t launch_mode(const AttnMaps& maps, const AttnArgs& a, cudaStream_t st) {
   static std::atomic<int> configured[64];
@@ -1091,6 +1114,14 @@ cudaError_t launch_mask_pack(const void* mask, int f16, int vec, int C, int T, l
     mask_pack_vec_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, nonbinary, tiles, tile_words);
   else
     mask_pack_kernel<<<grid, 256, 0, st>>>(mask, f16, C, T, ld, bits, words, nonbinary, tiles, tile_words);
+  ++t_launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_f16(const void* src, void* dst, long long nvec, unsigned* status, cudaStream_t st) {
+  const long long want = (nvec + 255) / 256;
+  const int grid = (int)(want < 152 * 8 ? want : 152 * 8);
+  convert_f16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec, status);
   ++t_launches;
   return cudaGetLastError();
 }

@@ -78,6 +78,10 @@ cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, int mode, cudaS
 cudaError_t launch_mask_pack(const void* mask, int f16, int vec, int C, int T, long long ld, uint32_t* bits,
                              int words, int* nonbinary, uint32_t* tiles, int tile_words, cudaStream_t st);
 
+// bf16 -> fp16, nvec 16-byte vectors (8 elements each); a value beyond fp16's range sets
+// ST_VRANGE in status
+cudaError_t launch_convert_f16(const void* src, void* dst, long long nvec, unsigned* status, cudaStream_t st);
+
 // bit copy of the chunk's K and V into the cache layout (one launch for both)
 cudaError_t launch_kv_relayout(const void* src_k, const void* src_v, void* dst_k, void* dst_v, int B, int C,
                                int H, int d, const long long ss[3], const long long ds[3], cudaStream_t st);

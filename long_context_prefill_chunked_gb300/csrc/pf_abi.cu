@@ -168,8 +168,12 @@ pf_status check_common(const pf_shape* sh, int32_t start_pos) {
     return fail(PF_EUNSUPPORTED, "start_pos %d is not a multiple of %d", start_pos, kTile);
   if ((long long)start_pos + sh->C > (1LL << 30)) return fail(PF_EINVAL, "sequence too long");
   if (!(sh->scale >= 0.f) || isinf(sh->scale)) return fail(PF_EINVAL, "bad scale");
+  if (sh->v_f16 != 0 && sh->v_f16 != 1) return fail(PF_EINVAL, "v_f16 must be 0 or 1 (got %d)", sh->v_f16);
   return PF_OK;
 }
+
+// Element type of v (v_hist, v_chunk, the sparse v and its pooled copy).
+pf_dtype v_type(const pf_shape* sh) { return sh->v_f16 ? PF_F16 : sh->in_dtype; }
 
 void fill_attn_common(const pf_shape* sh, int32_t start_pos, AttnArgs& a) {
   a.B = sh->B;
@@ -186,7 +190,7 @@ void fill_attn_common(const pf_shape* sh, int32_t start_pos, AttnArgs& a) {
   a.slots = (a.G % 2 == 0 && sh->d != 256) ? 2 : 1;
   a.n_hp = sh->Hq / a.slots;
   a.ab_type = sh->in_dtype == PF_BF16 ? 1 : 0;
-  a.convert_v = a.ab_type;
+  a.convert_v = v_type(sh) == PF_BF16 ? 1 : 0;  // P * V is fp16: a bf16 v is converted per tile
   const float scale = sh->scale > 0.f ? sh->scale : 1.0f / sqrtf((float)sh->d);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out_dtype = sh->out_dtype == PF_F32 ? 2 : (sh->out_dtype == PF_BF16 ? 1 : 0);
@@ -351,10 +355,12 @@ pf_status dense_entry(const pf_shape* sh, const void* q, const void* k_hist, con
   if ((rc = map_tokens(&maps.q, q, dt, B, C, Hq, d, qs, "q")) != PF_OK) return rc;
   const uint32_t kt_rows = (uint32_t)key_tile(d);
   if ((rc = map_tokens(&maps.kc, k_chunk, dt, B, C, Hkv, d, kcs, "k_chunk", kt_rows)) != PF_OK) return rc;
-  if ((rc = map_tokens(&maps.vc, v_chunk, dt, B, C, Hkv, d, kcs, "v_chunk", kt_rows)) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.vc, v_chunk, v_type(sh), B, C, Hkv, d, kcs, "v_chunk", kt_rows)) != PF_OK)
+    return rc;
   if (s > 0) {
     if ((rc = map_tokens(&maps.kh, k_hist, dt, B, s, Hkv, d, khs, "k_hist", kt_rows)) != PF_OK) return rc;
-    if ((rc = map_tokens(&maps.vh, v_hist, dt, B, s, Hkv, d, khs, "v_hist", kt_rows)) != PF_OK) return rc;
+    if ((rc = map_tokens(&maps.vh, v_hist, v_type(sh), B, s, Hkv, d, khs, "v_hist", kt_rows)) != PF_OK)
+      return rc;
   } else {
     maps.kh = maps.kc;
     maps.vh = maps.vc;
@@ -432,6 +438,17 @@ int64_t pf_launch_count(int32_t reset) {
   const long long n = t_launches;
   if (reset) t_launches = 0;
   return n;
+}
+
+pf_status pf_convert_f16(const void* src, void* dst, int64_t n, void* stream) {
+  if (src == nullptr || dst == nullptr) return fail(PF_EINVAL, "src and dst must not be NULL");
+  if (!aligned16(src) || !aligned16(dst)) return fail(PF_EINVAL, "src and dst must be 16-byte aligned");
+  if (n < 0 || n % 8 != 0) return fail(PF_EINVAL, "n (%lld) must be a non-negative multiple of 8", (long long)n);
+  if (n == 0) return PF_OK;
+  unsigned* status = status_words();
+  if (status == nullptr) return fail(PF_ECUDA, "no CUDA device (status words unavailable)");
+  cudaError_t e = launch_convert_f16(src, dst, n / 8, status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PF_OK : cuda_fail(e, "conversion launch");
 }
 
 pf_status pf_stream_status(void* stream) {
@@ -667,7 +684,7 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   float* vbar = static_cast<float*>(pooled);
   void* kbar_lp = sel->kbar + pe;  // the 16-bit round of the pooled keys written by pf_block_index
   void* vbar_lp = static_cast<char*>(pooled) + f32b + lpb;
-  const int bf16 = sh->in_dtype == PF_BF16 ? 1 : 0;
+  const int bf16 = v_type(sh) == PF_BF16 ? 1 : 0;  // v's type: pooled as read, copied in it
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   PoolArgs p{};
@@ -711,12 +728,12 @@ pf_status pf_attn_sparse(const pf_shape* sh, const void* q, const void* k, const
   if ((rc = map_tokens(&maps.q, q, dt, B, C, Hq, d, qs, "q")) != PF_OK) return rc;
   const uint32_t kt_rows = (uint32_t)key_tile(d);
   if ((rc = map_tokens(&maps.kh, k, dt, B, T, Hkv, d, ks, "k", kt_rows)) != PF_OK) return rc;
-  if ((rc = map_tokens(&maps.vh, v, dt, B, T, Hkv, d, ks, "v", kt_rows)) != PF_OK) return rc;
+  if ((rc = map_tokens(&maps.vh, v, v_type(sh), B, T, Hkv, d, ks, "v", kt_rows)) != PF_OK) return rc;
   // pooled [B, Hkv, nblk, d]: dims (d, nblk, Hkv, B), box 64 x 128 pooled rows
   if ((rc = make_map(&maps.kbar, kbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], kt_rows, 1,
                      "kbar")) != PF_OK)
     return rc;
-  if ((rc = make_map(&maps.vbar, vbar_lp, dt, d, nblk, Hkv, B, pst[2], pst[1], pst[0], kt_rows, 1,
+  if ((rc = make_map(&maps.vbar, vbar_lp, v_type(sh), d, nblk, Hkv, B, pst[2], pst[1], pst[0], kt_rows, 1,
                      "vbar")) != PF_OK)
     return rc;
   maps.kc = maps.kh;

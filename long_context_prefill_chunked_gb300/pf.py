@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "PF_OK", 1: "PF_EINVAL", 2: "PF_EUNSUPPORTED", 3: "PF_ECUDA",
 EXPORTS = ["pf_attn_dense", "pf_dense_workspace_bytes", "pf_dense_workspace_bytes_masked",
            "pf_attn_indexed", "pf_indexed_workspace_bytes",
            "pf_block_index", "pf_attn_sparse",
-           "pf_sparse_query_sizes",
+           "pf_sparse_query_sizes", "pf_convert_f16",
            "pf_stream_status", "pf_set_wait_timeout", "pf_set_debug_withhold", "pf_launch_count",
            "pf_last_error", "pf_version"]
 
@@ -49,7 +49,8 @@ class Shape(ctypes.Structure):
                 ("d", ctypes.c_int32), ("C", ctypes.c_int32), ("in_dtype", ctypes.c_int),
                 ("out_dtype", ctypes.c_int), ("mask_dtype", ctypes.c_int), ("scale", ctypes.c_float),
                 ("q_stride", I64x3), ("kh_stride", I64x3), ("kc_stride", I64x3),
-                ("o_stride", I64x3), ("okv_stride", I64x3), ("mask_ld", ctypes.c_int64)]
+                ("o_stride", I64x3), ("okv_stride", I64x3), ("mask_ld", ctypes.c_int64),
+                ("v_f16", ctypes.c_int32)]
 
 
 class Sel(ctypes.Structure):
@@ -93,6 +94,7 @@ def load() -> ctypes.CDLL:
     lib.pf_block_index.argtypes = [P(Shape), V, V, I32, I32, F, P(KeepRules), P(Sel), V]
     lib.pf_attn_sparse.argtypes = [P(Shape), V, V, V, I32, I32, P(Sel), V, V, V, V]
     lib.pf_sparse_query_sizes.argtypes = [P(Shape), I32, I32, P(SparseSizes)]
+    lib.pf_convert_f16.argtypes = [V, V, I64, V]
     lib.pf_stream_status.argtypes = [V]
     lib.pf_set_wait_timeout.argtypes = [I64]
     lib.pf_set_wait_timeout.restype = None
@@ -105,7 +107,7 @@ def load() -> ctypes.CDLL:
     for name in ("pf_attn_dense", "pf_dense_workspace_bytes", "pf_dense_workspace_bytes_masked",
                  "pf_attn_indexed", "pf_indexed_workspace_bytes",
                  "pf_block_index", "pf_attn_sparse",
-                 "pf_sparse_query_sizes", "pf_stream_status"):
+                 "pf_sparse_query_sizes", "pf_convert_f16", "pf_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -134,6 +136,12 @@ def _bth(t: torch.Tensor):
     if t.dim() != 4 or t.stride(3) != 1:
         raise ValueError("expected a [B, T, H, d] tensor with a contiguous last dim")
     return I64x3(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _same_layout(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """Equal strides wherever the extent is above 1 (a size-1 dimension's stride is never
+    used, and views of one-row slices keep their parent's)."""
+    return a.shape == b.shape and all(sa == sb or n == 1 for sa, sb, n in zip(a.stride(), b.stride(), a.shape))
 
 
 def _expect(t, shape, name, device):
@@ -171,6 +179,18 @@ def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _v_flag(q, k, v, name="v") -> int:
+    """k must have q's type; v either q's type or float16 (with bfloat16 q/k: the v_f16 mode,
+    in which the kernels read v as it is instead of converting each tile)."""
+    if k.dtype != q.dtype:
+        raise TypeError("k has dtype %s, q has %s" % (k.dtype, q.dtype))
+    if v.dtype == q.dtype:
+        return 0
+    if v.dtype == torch.float16 and q.dtype == torch.bfloat16:
+        return 1
+    raise TypeError("%s has dtype %s; expected %s or float16" % (name, v.dtype, q.dtype))
 
 
 def make_shape(q, k_like, out_dtype, scale=0.0) -> Shape:
@@ -277,16 +297,21 @@ def _dense_call(q, k_hist, v_hist, k_chunk, v_chunk, start_pos, mask, keep, out,
         raise ValueError("workspace is on %s, expected %s" % (workspace.device, dev))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     sh = make_shape(q, k_chunk, out.dtype, scale)
+    sh.v_f16 = _v_flag(q, k_chunk, v_chunk, "v_chunk")
+    if start_pos > 0 and (k_hist.dtype != k_chunk.dtype or v_hist.dtype != v_chunk.dtype):
+        raise TypeError("k_hist / v_hist must have the types of k_chunk / v_chunk")
+    if out_k is not None and (out_k.dtype != k_chunk.dtype or out_v.dtype != v_chunk.dtype):
+        raise TypeError("out_k / out_v must have the types of k_chunk / v_chunk")
     sh.kc_stride = _bth(k_chunk)
-    if v_chunk.stride() != k_chunk.stride():
+    if not _same_layout(v_chunk, k_chunk):
         raise ValueError("k_chunk and v_chunk must share strides")
     if start_pos > 0:
         sh.kh_stride = _bth(k_hist)
-        if v_hist.stride() != k_hist.stride():
+        if not _same_layout(v_hist, k_hist):
             raise ValueError("k_hist and v_hist must share strides")
     sh.o_stride = _bth(out)
     if out_k is not None:
-        if out_k.stride() != out_v.stride() or out_k.stride(3) != 1:
+        if not _same_layout(out_k, out_v) or out_k.stride(3) != 1:
             raise ValueError("out_k / out_v must share strides with a contiguous last dim")
         sh.okv_stride = I64x3(out_k.stride(0), out_k.stride(1), out_k.stride(2))  # (b, h, t)
     if mask is not None:
@@ -417,9 +442,10 @@ def attn_sparse(q, k, v, start_pos, sel: Selection, block=128, pooled=None, out=
         pooled = alloc_pooled(q, k, start_pos, block)
     if pooled.device != dev or pooled.numel() * pooled.element_size() < z.pooled_bytes:
         raise ValueError("pooled must hold %d bytes on %s" % (z.pooled_bytes, dev))
-    if v.stride() != k.stride():
+    if not _same_layout(v, k):
         raise ValueError("k and v must share strides")
     sh = make_shape(q, k, out.dtype, scale)
+    sh.v_f16 = _v_flag(q, k, v)
     sh.kh_stride = _bth(k)
     sh.o_stride = _bth(out)
     cs = sel.c_struct()
@@ -435,6 +461,20 @@ def vbar_view(pooled: torch.Tensor, q, k, start_pos, block=128, capacity=None) -
     B, Hkv, d = q.shape[0], k.shape[2], q.shape[3]
     cap = z.nblk if capacity is None else int(capacity)
     return pooled[: B * Hkv * cap * d * 4].view(torch.float32).view(B, Hkv, cap, d)
+
+
+def to_f16(x: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """bf16 -> fp16 copy of x (pf_convert_f16), for a v kept in fp16 (the v_f16 mode of the
+    attention calls).  x and out contiguous, numel a multiple of 8; a value beyond fp16's
+    range is reported by stream_status() as PF_ERANGE."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous bfloat16 tensor")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    if out.dtype != torch.float16 or not out.is_contiguous() or out.numel() != x.numel() or out.device != x.device:
+        raise ValueError("out must be a contiguous float16 tensor of x's size on x's device")
+    _check(load().pf_convert_f16(_ptr(x), _ptr(out), int(x.numel()), _stream(stream)))
+    return out
 
 
 def stream_status(stream=None):

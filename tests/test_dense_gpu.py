@@ -339,9 +339,10 @@ def test_lse_matches_oracle(case):
 def test_config4_dense_chunked_as_benchmarked(tmp_path):
     """The 32K prompt as bench.py runs it: 8 chunks of 4096 causal rows over the previous
     chunks' K/V, chunk outputs written into one [1, 32768, 32, 128] tensor, K/V emitted into a
-    head-major cache, the tail-split workspace on.  Per chunk 2048 seeded rows, the last 128 rows
-    and every tile-boundary row, all 32 heads, against the oracle (a process pool, one task per
-    chunk and KV head); the cache must be a bit copy."""
+    head-major cache, the tail-split workspace on, v kept in fp16 (each chunk's v converted once).
+    Per chunk 2048 seeded rows, the last 128 rows and every tile-boundary row, all 32 heads, against
+    the oracle (a process pool, one task per chunk and KV head); the cache must be a bit copy of
+    k and of the fp16 v."""
     import oracle_pool
     w = pi.config(4)
     N, CH = w.N, 4096
@@ -349,12 +350,15 @@ def test_config4_dense_chunked_as_benchmarked(tmp_path):
     Q, K, V = to(w.q), to(w.k), to(w.v)
     out = torch.empty((1, N, 32, 128), dtype=torch.float32, device="cuda")
     ck = torch.empty((1, 8, N, 128), dtype=torch.bfloat16, device="cuda")
-    cv = torch.empty_like(ck)
+    cv = torch.empty((1, 8, N, 128), dtype=torch.float16, device="cuda")
+    V16 = torch.empty(V.shape, dtype=torch.float16, device="cuda")
     for s in range(0, N, CH):
-        pfx.attn_dense(Q[:, s:s + CH], K[:, :s], V[:, :s], K[:, s:s + CH], V[:, s:s + CH], s,
+        pfx.to_f16(V[:, s:s + CH], out=V16[:, s:s + CH])
+        pfx.attn_dense(Q[:, s:s + CH], K[:, :s], V16[:, :s], K[:, s:s + CH], V16[:, s:s + CH], s,
                        out=out[:, s:s + CH], out_k=ck[:, :, s:s + CH], out_v=cv[:, :, s:s + CH])
     pfx.stream_status()
-    assert torch.equal(ck.transpose(1, 2).contiguous(), K) and torch.equal(cv.transpose(1, 2).contiguous(), V)
+    assert torch.equal(ck.transpose(1, 2).contiguous(), K)
+    assert torch.equal(cv.transpose(1, 2).contiguous(), V16)  # the cache holds the fp16 v bit for bit
     root = str(tmp_path)
     oracle_pool.save_inputs(w, root)
     tasks = []

@@ -10,7 +10,9 @@ compared, near-threshold rows included: a GPU row selection may differ from the
 oracle's only at near-threshold pairs, and where it does the expected output is the
 oracle's under that (equally valid) selection.  The oracle runs in a pool of worker
 processes, one task per (chunk, KV head, path).  The sparse path keeps one pooled-key buffer
-and one workspace for the whole prompt, so each chunk pools only its own blocks.
+and one workspace for the whole prompt, so each chunk pools only its own blocks.  As in the
+benchmark, v is kept in fp16: each path converts each chunk's bf16 v once (pf_convert_f16)
+and the kernels read the fp16 v; the head-major cache holds k in bf16 and v in fp16.
 """
 import numpy as np
 import pytest
@@ -65,7 +67,10 @@ def test_config5_every_chunk_dense_and_sparse(tmp_path):
     oracle_pool.save_inputs(w, root)
     Q, K, V = dev(w.q, w.dtype), dev(w.k, w.dtype), dev(w.v, w.dtype)
     cache_k = torch.empty((1, Hkv, N, d), dtype=Q.dtype, device="cuda")
-    cache_v = torch.empty_like(cache_k)
+    cache_v = torch.empty(cache_k.shape, dtype=torch.float16, device="cuda")
+    # v kept in fp16 as the benchmark keeps it: each path converts each chunk's v once
+    V16d = torch.empty(V.shape, dtype=torch.float16, device="cuda")
+    V16s = torch.empty_like(V16d)
     # the pooled keys and values of the history are kept from chunk to chunk: one buffer each
     # for the whole prompt, and every call pools only its own chunk's blocks
     kbar = pfx.alloc_kbar(Q[:, :CH], K, N)
@@ -76,11 +81,13 @@ def test_config5_every_chunk_dense_and_sparse(tmp_path):
         rows = sample_rows(CH, 2048, 500 + c)
         ridx = torch.from_numpy(rows).cuda()
         q = Q[:, s:s + CH]
-        out_d = pfx.attn_dense(q, K[:, :s], V[:, :s], K[:, s:s + CH], V[:, s:s + CH], s,
+        pfx.to_f16(V[:, s:s + CH], out=V16d[:, s:s + CH])
+        out_d = pfx.attn_dense(q, K[:, :s], V16d[:, :s], K[:, s:s + CH], V16d[:, s:s + CH], s,
                                out_k=cache_k[:, :, s:s + CH], out_v=cache_v[:, :, s:s + CH])
         sel = pfx.alloc_selection(q, K[:, :s + CH], s, kbar=kbar, pooled_blocks=s // w.block)
         pfx.block_index(q, K[:, :s + CH], s, w.block, w.alpha, sel=sel)
-        out_s = pfx.attn_sparse(q, K[:, :s + CH], V[:, :s + CH], s, sel, pooled=pooled)
+        pfx.to_f16(V[:, s:s + CH], out=V16s[:, s:s + CH])
+        out_s = pfx.attn_sparse(q, K[:, :s + CH], V16s[:, :s + CH], s, sel, pooled=pooled)
         pfx.stream_status()
         oracle_pool.save_result(root, "dense", s, rows, out_d[0, ridx].cpu().numpy())
         oracle_pool.save_result(root, "sparse", s, rows, out_s[0, ridx].cpu().numpy(),
@@ -96,8 +103,8 @@ def test_config5_every_chunk_dense_and_sparse(tmp_path):
         del out_d, out_s, sel
     # the cache holds every chunk's K/V, bit for bit
     assert torch.equal(cache_k[0].transpose(0, 1), K[0])
-    assert torch.equal(cache_v[0].transpose(0, 1), V[0])
-    del Q, K, V, cache_k, cache_v, kbar, pooled
+    assert torch.equal(cache_v[0].transpose(0, 1), V16d[0])  # the cache holds the fp16 v bit for bit
+    del Q, K, V, V16d, V16s, cache_k, cache_v, kbar, pooled
     torch.cuda.empty_cache()
     # planted structure: the executed (tile-union) skip share over the whole prompt
     share = 1.0 - kept_tiles / cand_tiles
