@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int sl = 0; sl < a.slots; ++sl)
         for (int c = 0; c < nd; ++c)
           tma_load_4d_w(sb + SM_Q + 32768u * sl + 16384u * c, &maps.q, BAR(B_Q), 64 * c, h0 + sl,
-                      q0, b);
+                        q0, b);
       int last_k[NSK], last_v[NSV];
       for (int st = 0; st < NSK; ++st) last_k[st] = -1;
       for (int st = 0; st < NSV; ++st) last_v[st] = -1;
@@ -409,8 +409,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // tile j reuses the K stage of tile j - 2 and the V stage of tile j - 3: both freed by
         // issue iteration j - 2 (B_TD + (j - 2) % NTD, its ((j - 2) / NTD)-th phase; the next
         // phase of that barrier needs tile j + 2 loaded first, so it cannot be ahead)
-        if (j >= 2 && !wait_all(BAR(B_TD + (j - 2) % NTD), (uint32_t)((j - 2) / NTD) & 1u, a.timeout, abort_flag,
-                                a.status, (R_PROD << 8) | (B_TD + (j - 2) % NTD)))
+        const int td = (j - 2) % NTD;
+        if (j >= 2 && !wait_all(BAR(B_TD + td), (uint32_t)((j - 2) / NTD) & 1u, a.timeout, abort_flag, a.status,
+                                (R_PROD << 8) | (B_TD + td)))
           break;
         mbar_arrive_expect_tx_w(BAR(B_KF + st), tile_bytes);
         for (int c = 0; c < nd; ++c)
@@ -455,7 +456,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
           mma_ts_w(d_tmem, tmem + 256u * sl + 8u * kk, bv + ((2048u * kk) >> 4), idesc_pv,
-                 (acc || kk > 0) ? 1u : 0u);
+                   (acc || kk > 0) ? 1u : 0u);
       };
       const int vbar_first = a.convert_v ? B_VC : B_VF;
       bool ok = wait_all(BAR(B_Q), 0, a.timeout, abort_flag, a.status, (R_MMA << 8) | B_Q);
