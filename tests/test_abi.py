@@ -63,6 +63,7 @@ def dense(lib, sh, q=FAKE, kh=None, vh=None, kc=FAKE, vc=FAKE, mask=None, s=0, o
     (dict(C=0), pf.PF_EINVAL),
     (dict(in_dtype=pf.PF_F32), pf.PF_EUNSUPPORTED),
     (dict(scale=-1.0), pf.PF_EINVAL),
+    (dict(v_f16=2), pf.PF_EINVAL),
 ])
 def test_dense_rejects_bad_shapes(lib, kw, code):
     assert dense(lib, shape(**kw)) == code
@@ -256,3 +257,28 @@ def test_package_exports_every_binding_function():
               and f.__module__ == mod.__name__ and n != "make_shape"]
     missing = [n for n in public if not hasattr(pkg, n)]
     assert not missing, missing
+
+
+def test_binding_v_type_and_layout_rules():
+    """The binding's v type rule (v in q's type, or fp16 with bf16 q/k: the v_f16 flag) and its
+    stride comparison (size-1 dimensions ignored: a one-row batch view keeps its parent's
+    batch stride)."""
+    import torch
+    bq = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
+    assert pf._v_flag(bq, bq, bq) == 0
+    assert pf._v_flag(bq, bq, bq.half()) == 1
+    hq = bq.half()
+    assert pf._v_flag(hq, hq, hq) == 0
+    with pytest.raises(TypeError):
+        pf._v_flag(bq, bq, bq.float())
+    with pytest.raises(TypeError):
+        pf._v_flag(bq, bq.half(), bq)
+    with pytest.raises(TypeError):
+        pf._v_flag(hq, hq, bq)
+    big = torch.zeros(1, 12, 2, 64, dtype=torch.bfloat16)
+    view = big[:, 4:8]                  # batch stride 12*2*64, the fresh tensor's is 4*2*64
+    fresh = torch.zeros(1, 4, 2, 64, dtype=torch.float16)
+    assert view.stride(0) != fresh.stride(0) and pf._same_layout(view, fresh)
+    two = torch.zeros(2, 12, 2, 64, dtype=torch.bfloat16)[:, 4:8]
+    assert not pf._same_layout(two, torch.zeros(2, 4, 2, 64, dtype=torch.float16))
+    assert not pf._same_layout(fresh, fresh.transpose(1, 2))
