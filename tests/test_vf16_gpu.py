@@ -127,9 +127,22 @@ def test_indexed_fp16_v_bit_identical(w):
     assert torch.equal(out, ref)
 
 
-@pytest.mark.parametrize("s,C", [(0, 1536), (512, 1024)])
-def test_sparse_fp16_v_matches_oracle(s, C):
-    w = pi.planted_workload("vf16-sparse", 65, 1, 4, 2, 128, 1536, 1536, "bf16")
+def test_dense_fp16_v_head_dim_256():
+    """Head dim 256 (64-key tiles, one head per CTA): fp16 v equals the bf16-v call bit for bit."""
+    w = pi.normal_workload("vf16-d256", 66, 1, 4, 2, 256, 768, 437, "bf16")
+    s, C = 256, 437
+    q = dev(w.q[:, s:s + C], "bf16")
+    kh, kc = dev(w.k[:, :s], "bf16"), dev(w.k[:, s:s + C], "bf16")
+    vh, vc = dev(w.v[:, :s], "bf16"), dev(w.v[:, s:s + C], "bf16")
+    ref = pfx.attn_dense(q, kh, vh, kc, vc, s)
+    out = pfx.attn_dense(q, kh, pfx.to_f16(vh.contiguous()), kc, pfx.to_f16(vc.contiguous()), s)
+    pfx.stream_status()
+    assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("s,C,d", [(0, 1536, 128), (512, 1024, 128), (512, 1024, 256)])
+def test_sparse_fp16_v_matches_oracle(s, C, d):
+    w = pi.planted_workload("vf16-sparse", 65, 1, 4, 2, d, 1536, 1536, "bf16")
     C = min(C, w.N - s)
     q = dev(w.q[:, s:s + C], "bf16")
     k = dev(w.k[:, :s + C], "bf16")
