@@ -51,13 +51,18 @@ def flops_equiv(C, s, Hq=HQ, d=D):
 
 
 def kernel_source_hash():
-    """sha256 over the sources that define the dense attention kernel (a stored ncu traffic
-    figure is only reported while it still matches)."""
+    """sha256 over the code of the sources that define the dense attention kernel, comments and
+    whitespace removed (a stored ncu traffic figure is only reported while the code it was
+    measured on is unchanged; editing a comment does not change the kernel)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("attn_fwd.cu", "kernels.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "long_context_prefill_chunked_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "long_context_prefill_chunked_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", "", src)                 # line comments (no string here holds //)
+        h.update(re.sub(r"\s+", "", src).encode())
     return h.hexdigest()
 
 

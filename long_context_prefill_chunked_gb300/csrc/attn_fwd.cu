@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr uint32_t O_COL = WIDE ? 256u : 128u;  // O's first column in the slot's tensor memory
   constexpr uint32_t KBOX = KT * 128u;         // bytes of one 64-column box of a K / V tile
   // a packed explicit mask is launched as bits, then as values: the launch that does not match
-  // the packing pass's verdict returns before it touches anything (the whole CTA alike)
+  // the packing pass's decision returns before it touches anything (the whole CTA alike)
   if (MODE == MODE_MASKB && __ldg(a.mask_nonbinary) != 0) return;
   if (MODE == MODE_MASK && a.mask_nonbinary != nullptr && __ldg(a.mask_nonbinary) == 0) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];

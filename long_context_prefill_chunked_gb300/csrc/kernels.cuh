@@ -13,7 +13,7 @@ constexpr int kMaxSplit = 8;      // parts of one split dense unit (tail split)
 constexpr int kAttnThreads = 384; // 8 softmax warps (2 slots x 4), TMA warp, MMA warp, 2 V converters
 
 // MODE_MASKB: an explicit mask read as the packing pass's bits.  A packed mask is launched
-// twice, MODE_MASKB then MODE_MASK; each launch returns at once unless the pass's verdict on
+// twice, MODE_MASKB then MODE_MASK; each launch returns at once unless the pass's decision on
 // the mask (binary or not) is its own, so each keeps its own register allocation.
 enum AttnMode : int { MODE_CAUSAL = 0, MODE_MASK = 1, MODE_SPARSE = 2, MODE_MASKB = 3 };
 

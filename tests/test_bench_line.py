@@ -35,3 +35,23 @@ def test_reference_arm_prints_one_contract_line(monkeypatch):
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_traffic_stamp_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    """The stored ncu traffic figure is voided by a change to the kernel's code, not by an
+    edited comment or re-indented line."""
+    import shutil
+    import bench
+    src = os.path.join(bench.ROOT, "long_context_prefill_chunked_gb300", "csrc")
+    dst = tmp_path / "long_context_prefill_chunked_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for f in ("attn_fwd.cu", "kernels.cuh", "ptx.cuh"):
+        shutil.copy(os.path.join(src, f), dst / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    p = dst / "ptx.cuh"
+    text = p.read_text()
+    p.write_text("// an added comment\n/* and a block\n comment */\n" + text.replace("\n", "\n  ", 3))
+    assert bench.kernel_source_hash() == h0
+    p.write_text(text + "\nstatic int pf_probe_extra_symbol;\n")
+    assert bench.kernel_source_hash() != h0
