@@ -291,9 +291,14 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         if (lane == 0) mbar_arrive(XB(I_SE + 2 * sl + ub));
         const int lim = ob - pt * PT;  // columns c < lim are candidates
         if (pass == 0) {
+          if (lim >= PT) {  // every column a candidate (all but a row's last pooled tile)
 #pragma unroll
-          for (int c = 0; c < PT; ++c)
-            if (c < lim) smax = fmaxf(smax, __uint_as_float(xr[c]));
+            for (int c = 0; c < PT; ++c) smax = fmaxf(smax, __uint_as_float(xr[c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < PT; ++c)
+              if (c < lim) smax = fmaxf(smax, __uint_as_float(xr[c]));
+          }
         } else {
           // exp((s - smax) * scale) >= alpha  <=>  s >= smax + ln(alpha) / scale  (scale > 0): one
           // compare per column; the two roundings differ by about 1e-6 relative in the ratio, far
@@ -303,10 +308,9 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           for (int q = 0; q < PT / 32; ++q) {
             uint32_t word = 0u;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int c = 32 * q + i;
-              if (c < lim && __uint_as_float(xr[c]) >= thr) word |= 1u << i;
-            }
+            for (int i = 0; i < 32; ++i)
+              if (__uint_as_float(xr[32 * q + i]) >= thr) word |= 1u << i;
+            word &= range_bits(pt * (PT / 32) + q, 0, ob);  // columns past the candidates
             const int w = pt * (PT / 32) + q;
             // keep rules on this word's candidates (blocks below ob): sinks, the local
             // window, the dense tail; then the 32-row query tile's union (a warp's rows are
