@@ -13,7 +13,9 @@
 // into kbar_hi = bf16(kbar) and kbar_lo = bf16(kbar - kbar_hi) and each score is
 // accumulated in fp32 tensor memory as q . kbar_hi + q . kbar_lo (q is bf16 and
 // exact).  Pass 1 streams every pooled tile (128 blocks; 64 at head dim 256) once
-// to find the row maximum, pass 2 streams them again and thresholds.
+// to find the row maximum, pass 2 streams them again and thresholds.  A unit with
+// at most two pooled tiles keeps pass 1's scores in its two tensor-memory buffers
+// and pass 2 reads them again instead of recomputing them.
 //
 // One CTA = (batch, 128-row query tile, `slots` query heads of one KV group):
 //   warps 0-3 / 4-7  row threads of slot 0 / 1 (thread t owns row t = TMEM lane t)
@@ -84,7 +86,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 // keep their phases from unit to unit, and the next unit's Q tile is loaded as soon as the
 // previous unit's last MMA has read Q (I_QE), while its rows are still being thresholded.
 struct IndexUnit {
-  int b, h0, g, qt, q0, ob, np, nsteps;
+  int b, h0, g, qt, q0, ob, np, nsteps, msteps;
+  bool reuse;  // np <= 2: pass 1's scores stay in the two score buffers for pass 2
 };
 
 template <int PT>
@@ -99,7 +102,11 @@ __device__ __forceinline__ IndexUnit index_unit(const IndexArgs& a, int u) {
   x.q0 = x.qt * kTile;
   x.ob = (a.s + x.q0) / kTile;        // diagonal block; candidates 0 .. ob-1
   x.np = (x.ob + PT - 1) / PT;        // pooled tiles holding the candidates
-  x.nsteps = 2 * x.np;                // pass 1 and pass 2
+  x.nsteps = 2 * x.np;                // row steps: pass 1 and pass 2
+  // With at most two pooled tiles the slot's two score buffers hold every score of the row, so
+  // pass 2 reads pass 1's scores again instead of recomputing them: np MMA steps, not 2 np.
+  x.reuse = x.np <= 2;
+  x.msteps = x.reuse ? x.np : x.nsteps;
   return x;
 }
 
@@ -188,7 +195,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           for (int c = 0; c < nd; ++c)
             tma_load_4d(sb + X_Q + 32768u * sl + box * c, &maps.q, XB(I_Q), 64 * c, x.h0 + sl, x.q0, x.b);
         last_q = qloads++;
-        for (int t = 0; t < x.nsteps; ++t, ++tg) {
+        for (int t = 0; t < x.msteps; ++t, ++tg) {
           const int st = (int)(tg % XST), use = (int)(tg / XST);
           const int pt = t % x.np;
           if (use > 0 && !(ok = mbar_wait(XB(I_KE + st), (uint32_t)(use - 1) & 1u, a.timeout, abort_flag,
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
         ++qloads;
         if (!ok) break;
         tc_fence_after();
-        for (int t = 0; ok && t < x.nsteps; ++t, ++tg) {
+        for (int t = 0; ok && t < x.msteps; ++t, ++tg) {
           const int st = (int)(tg % XST), ub = (int)(tg % 2);
           ok = wait_all(XB(I_KF + st), (uint32_t)(tg / XST) & 1u, a.timeout, abort_flag, a.status,
                         (R_MMA << 8) | (I_KF + st));
@@ -276,19 +283,29 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       const uint32_t dbit = 1u << (ob & 31);
       float smax = -INFINITY;
       const bool tail_row = a.s + row >= a.tail_from;  // dense-tail rule: keep every candidate
-      for (int t = 0; t < x.nsteps; ++t, ++tg) {
-        const int ub = (int)(tg % 2), pass = t / np, pt = t % np;
-        ok = wait_all(XB(I_SF + 2 * sl + ub), (uint32_t)(tg / 2) & 1u, a.timeout, abort_flag, a.status,
-                      (R_ROW << 8) | (I_SF + 2 * sl + ub));
-        if (!ok) break;
-        tc_fence_after();
+      const long long tg0 = tg;  // this unit's first MMA step
+      for (int t = 0; t < x.nsteps; ++t) {
+        const int pass = t / np, pt = t % np;
+        // the MMA step whose scores this row step reads: step t, or with reuse the pass-1 step
+        // of the same pooled tile
+        const long long m = x.reuse ? tg0 + pt : tg0 + t;
+        const int ub = (int)(m % 2);
+        const bool fresh = !x.reuse || pass == 0;  // scores not read yet: wait for the MMAs
+        if (fresh) {
+          ok = wait_all(XB(I_SF + 2 * sl + ub), (uint32_t)(m / 2) & 1u, a.timeout, abort_flag, a.status,
+                        (R_ROW << 8) | (I_SF + 2 * sl + ub));
+          if (!ok) break;
+          tc_fence_after();
+        }
         uint32_t xr[PT];
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + 256u * sl + 128u * ub;
         if constexpr (PT == 128) tmem_ld128_wait(taddr, xr);
         else tmem_ld64_wait(taddr, xr);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(XB(I_SE + 2 * sl + ub));
+        // the buffer is free once its last reader has loaded it (with reuse: in pass 2); one
+        // release per MMA step either way
+        if (lane == 0 && (!x.reuse || pass == 1)) mbar_arrive(XB(I_SE + 2 * sl + ub));
         const int lim = ob - pt * PT;  // columns c < lim are candidates
         if (pass == 0) {
           if (lim >= PT) {  // every column a candidate (all but a row's last pooled tile)
@@ -329,6 +346,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
           }
         }
       }
+      tg = tg0 + x.msteps;
       if (ok) {
         // words past the pooled tiles: only the diagonal bit
         for (int w = (PT / 32) * np; w < a.words; ++w) {
