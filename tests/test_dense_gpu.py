@@ -278,17 +278,17 @@ def test_binary_mask_past_the_tile_bitmap_visits_every_tile():
 
 
 def test_binary_mask_tile_bitmap_above_1024_tiles():
-    """start_pos + C = 150201 keys is 1174 key tiles (the last one 57 keys long): a query tile's
+    """start_pos + C = 150088 keys is 1173 key tiles (the last one 72 keys long): a query tile's
     bitmap spans 37 words, and the kept tiles past tile 1024 land in the packing pass's second
     per-lane bitmap word.  Query tile 0 keeps tiles 3, 1100 and the ragged last one, query tile 1
     keeps tiles 500 and 1050; a bit lost from the bitmap drops a kept tile.  Sampled rows of both
     query tiles against the oracle."""
-    C, s = 200, 150001
+    C, s = 200, 149888
     T = s + C
     w = pi.normal_workload("tile-bitmap-hi", 85, 1, 2, 1, 128, T, C, "bf16")
     g = np.random.default_rng(86)
     mask = np.full((C, T), -30000.0, dtype=np.float32)
-    for (r0, r1), kept in (((0, 128), (3, 1100, 1173)), ((128, C), (500, 1050))):
+    for (r0, r1), kept in (((0, 128), (3, 1100, 1172)), ((128, C), (500, 1050))):
         for t in kept:
             blk = mask[r0:r1, t * 128:min(T, t * 128 + 128)]
             blk[g.random(blk.shape) < 0.6] = 0.0
@@ -296,7 +296,7 @@ def test_binary_mask_tile_bitmap_above_1024_tiles():
     rows = np.array([0, 5, 77, 127, 128, 160, 199])
     out, _, _ = run_chunk(w, s, mask)
     ref = ref_chunk(w, s, mask, rows=rows)
-    assert_close(out[:, rows], ref, "1174 key tiles")
+    assert_close(out[:, rows], ref, "1173 key tiles")
 
 
 @pytest.mark.parametrize("mdtype", [np.float32, np.float16])
