@@ -277,6 +277,21 @@ def test_binary_mask_past_the_tile_bitmap_visits_every_tile():
     assert_close(out[:, rows], ref, "2050 key tiles")
 
 
+@pytest.mark.parametrize("kind", ["binary", "values"])
+def test_mask_broadcast_over_batch(kind):
+    """A [C, s + C] mask applies to every batch and head: batch 2, a ragged chunk over a
+    history, the mask read as bits with dropped key tiles skipped (binary) or as values."""
+    C, s = 300, 256
+    w = pi.normal_workload("mask-batch", 87, 2, 4, 2, 128, s + C, C, "bf16")
+    if kind == "binary":
+        mask = _tile_sparse_mask(88, C, s + C, [2, 3, 5])
+    else:
+        g = np.random.default_rng(89)
+        mask = np.where(g.random((C, s + C)) < 0.3, -30000.0, g.normal(0.0, 2.0, (C, s + C))).astype(np.float32)
+    out, _, _ = run_chunk(w, s, mask)
+    assert_close(out, ref_chunk(w, s, mask), "batch 2, %s mask" % kind)
+
+
 def test_binary_mask_tile_bitmap_above_1024_tiles():
     """start_pos + C = 150088 keys is 1173 key tiles (the last one 72 keys long): a query tile's
     bitmap spans 37 words, and the kept tiles past tile 1024 land in the packing pass's second

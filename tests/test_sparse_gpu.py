@@ -113,6 +113,30 @@ def test_small_planted_selection_and_output(small, s, C):
     assert oracle.skip_share(osel) > 0.5
 
 
+# shapes the block-sparse path takes besides the benchmark's: head dim 64, fp16 inputs, batch 2,
+# and odd or unit query-head groups (one head per CTA at head dim 128, no head pairing)
+SHAPES = [
+    (2, 4, 2, 64, "f16", 512, 700),
+    (1, 3, 1, 128, "bf16", 256, 900),
+    (1, 2, 2, 128, "f16", 0, 1100),
+    (2, 8, 2, 128, "bf16", 1024, 1024),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,dtype,s,C", SHAPES)
+def test_sparse_shapes_dtypes_and_batches(B, Hq, Hkv, d, dtype, s, C):
+    """Selection (row bits and tile lists) and output against the oracle, every row of every
+    batch and head, for a planted prompt of each shape; ragged chunks over a history."""
+    w = pi.planted_workload("sparse-shape-%d-%d-%d-%d-%s" % (B, Hq, Hkv, d, dtype), 31 + d + Hq,
+                            B, Hq, Hkv, d, s + C, C, dtype, beta=14.0)
+    q, k, v, sel, pooled, out = run_sparse(w, s, C, 0.1)
+    ref, osel, gk = expected_sparse(w, s, C, 0.1, np.arange(C), sel)
+    check_selection(osel, gk)
+    check_tile_lists(sel, osel, C)
+    assert_rows_close(out, ref, "B %d Hq %d Hkv %d d %d %s" % (B, Hq, Hkv, d, dtype))
+    assert oracle.skip_share(osel) > 0.3
+
+
 def test_near_threshold_pairs_on_the_gpu(small):
     """alpha is set to one candidate's own probability ratio (rounded to fp32), so that pair --
     and any other within 1e-4 relative -- sits in the threshold band.  The GPU may decide it
