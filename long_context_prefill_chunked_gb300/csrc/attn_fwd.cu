@@ -554,8 +554,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bits_row = a.row_bits + ((long long)(b * a.Hq + h) * a.C + row) * a.words;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    // MODE_MASKB: one 16-byte (8-byte for 64-key tiles) word group of mask bits per row and
-    // key tile, loaded before the step's score wait (padding rows read none and mask nothing).
+    // MODE_MASKB: the tile's mask bits, one 16-byte word group per row and 128-key group (bit L of
+    // word c = key 4L + c), loaded before the step's score wait (padding rows read none and mask
+    // nothing).  In registers, key 4L + c of a KT-key tile is bit (c * KT / 4 + L) of the tile's
+    // KT / 32 words: a 64-key tile takes its 16-bit half of each of its group's four words.
     // Loading a step ahead instead holds four more registers across the loop and spills: slower.
     const uint32_t* mbits = nullptr;
     if (MODE == MODE_MASKB && valid) mbits = a.mask_bits + (long long)row * a.mask_words;
@@ -576,9 +578,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             wq[2] = bw.z;
             wq[3] = bw.w;
           } else {
-            const uint2 bw = __ldg(reinterpret_cast<const uint2*>(mbits) + kt);
-            wq[0] = bw.x;
-            wq[1] = bw.y;
+            const uint4 bw = __ldg(reinterpret_cast<const uint4*>(mbits) + (kt >> 1));
+            const uint32_t sel = (kt & 1) ? 0x7632u : 0x5410u;  // high or low halves
+            wq[0] = __byte_perm(bw.x, bw.y, sel);
+            wq[1] = __byte_perm(bw.z, bw.w, sel);
           }
         }
       }
@@ -606,8 +609,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int q = 0; q < KT / 32; ++q)
           if (wq[q] != 0xffffffffu) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (!((wq[q] >> i) & 1u)) x[32 * q + i] = -INFINITY;
+            for (int i = 0; i < 32; ++i) {
+              // bit i of word q is key 4L + c with c * KT / 4 + L = 32q + i
+              constexpr int kL = KT / 4;
+              const int c = (32 * q + i) / kL, L = (32 * q + i) % kL;
+              if (!((wq[q] >> i) & 1u)) x[4 * L + c] = -INFINITY;
+            }
           }
       } else if (MODE == MODE_MASK) {
         xs = 1.f;
@@ -876,13 +883,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #undef BAR
 }
 
-// One CTA per mask row (rows past 65535 loop): warp-wide loads of 32 consecutive values
-// become one word through a ballot; each warp loads kPackUnroll consecutive words before it
-// ballots them, so that many loads are in flight (the pass is bound by reading the mask); the
-// row's kept count decides whether a fully dropped row (a plain softmax over the raw scores with
-// values, NaN with bits) forces the value path; the key tiles the row keeps are ORed into its
-// query tile's tile bitmap (when tiles != null).
-constexpr int kPackUnroll = 8;
+// Packed mask bits: per row, four words per 128-key tile; bit L of word c is key 4L + c of the
+// tile (set = kept, value 0).  It is the layout four warp ballots give when lane L holds keys
+// 4L .. 4L + 3, one ballot per c, so the packing needs no shuffles.
+//
+// One CTA per mask row (rows past 65535 loop): lane L loads keys 4L + c of a tile (four scalar
+// loads; for rows not on 16-byte boundaries) and each warp keeps kPackTiles tiles in flight
+// before their ballots (the pass reads the mask once); the row's kept count decides whether a
+// fully dropped row (a plain softmax over the raw scores with values, NaN with bits) forces the
+// value path; the key tiles the row keeps are ORed into its query tile's tile bitmap (when
+// tiles != null).
+constexpr int kPackTiles = 2;
 __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__ mask, int f16, int C,
                                                         int T, long long ld, uint32_t* __restrict__ bits,
                                                         int words, int* nonbinary, uint32_t* tiles,
@@ -891,36 +902,43 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__
   __shared__ uint32_t row_tiles[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x / 32;
+  const int groups = words / 4;  // 128-key tiles per row
   for (int row = blockIdx.y; row < C; row += gridDim.y) {
     if (threadIdx.x == 0) kept_any = 0;
     for (int t = threadIdx.x; t < 64; t += blockDim.x) row_tiles[t] = 0u;
     __syncthreads();
     bool nonbin = false, any = false;
-    for (int w0 = warp * kPackUnroll; w0 < words; w0 += nwarps * kPackUnroll) {
-      float v[kPackUnroll];
+    for (int m0 = warp * kPackTiles; m0 < groups; m0 += nwarps * kPackTiles) {
+      float v[kPackTiles][4];
 #pragma unroll
-      for (int u = 0; u < kPackUnroll; ++u) {  // every load first, then the ballots
-        const int key = (w0 + u) * 32 + lane;
-        v[u] = 0.f;
-        if (w0 + u < words && key < T) {
-          const long long o = (long long)row * ld + key;
-          v[u] = f16 ? __half2float(reinterpret_cast<const __half*>(mask)[o])
-                     : reinterpret_cast<const float*>(mask)[o];
+      for (int u = 0; u < kPackTiles; ++u) {  // every load first, then the ballots
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int key = (m0 + u) * kTile + 4 * lane + c;
+          v[u][c] = 0.f;
+          if (m0 + u < groups && key < T) {
+            const long long o = (long long)row * ld + key;
+            v[u][c] = f16 ? __half2float(reinterpret_cast<const __half*>(mask)[o])
+                          : reinterpret_cast<const float*>(mask)[o];
+          }
         }
       }
 #pragma unroll
-      for (int u = 0; u < kPackUnroll; ++u) {
-        const int w = w0 + u;
-        if (w >= words) break;  // uniform across the warp
-        const bool inb = w * 32 + lane < T;
-        const bool keep = inb && v[u] == 0.f;
-        nonbin |= inb && !(v[u] == 0.f || v[u] <= -10000.f);
-        const uint32_t word = __ballot_sync(0xffffffffu, keep);
-        any |= word != 0u;
-        if (lane == 0) {
-          bits[(long long)row * words + w] = word;
-          if (tiles != nullptr && word != 0u) atomicOr(&row_tiles[(w >> 2) >> 5], 1u << ((w >> 2) & 31));
+      for (int u = 0; u < kPackTiles; ++u) {
+        const int m = m0 + u;
+        if (m >= groups) break;  // uniform across the warp
+        uint32_t wc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const bool inb = m * kTile + 4 * lane + c < T;
+          nonbin |= inb && !(v[u][c] == 0.f || v[u][c] <= -10000.f);
+          wc[c] = __ballot_sync(0xffffffffu, inb && v[u][c] == 0.f);
         }
+        if (lane == 0)
+          *reinterpret_cast<uint4*>(bits + (long long)row * words + 4 * m) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
+        const bool tile_kept = (wc[0] | wc[1] | wc[2] | wc[3]) != 0u;
+        any |= tile_kept;
+        if (lane == 0 && tiles != nullptr && tile_kept) atomicOr(&row_tiles[m >> 5], 1u << (m & 31));
       }
     }
     if (__any_sync(0xffffffffu, any) && lane == 0) kept_any = 1;
@@ -935,11 +953,11 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const void* __restrict__
 }
 
 // The same packing for masks whose rows start on 16-byte boundaries (the common case): each lane
-// reads four consecutive keys with one streaming vector load (16 bytes of fp32, 8 of fp16), so a
-// warp covers one 128-key tile per load and keeps kPackGroups tiles in flight.  Lane L holds keys
-// 4L .. 4L + 3 of the tile, i.e. bits 4(L mod 8) .. 4(L mod 8) + 3 of the tile's word L / 8; three
-// xor-shuffles inside each group of eight lanes assemble the four words, and one vote gives the
-// tile's "some key kept" bit.  Bits, flags and tile bitmap are those of mask_pack_kernel.
+// reads its four keys 4L .. 4L + 3 with one streaming vector load (16 bytes of fp32, 8 of fp16),
+// so a warp covers one 128-key tile per load and keeps kPackGroups tiles in flight; the four
+// ballots are the tile's four words.  The pass is bound by its instructions more than by the
+// mask's bytes, so a tile wholly inside the row skips the per-key bounds tests.  Bits, flags and
+// tile bitmap are those of mask_pack_kernel.
 constexpr int kPackGroups = 4;
 // The first n (< 4) mask values from element o on, one scalar load each; the rest 0.  Kept out of
 // line: inlined, its per-key branches cost the packing kernel a stack frame.
@@ -958,7 +976,6 @@ __global__ void __launch_bounds__(256) mask_pack_vec_kernel(const void* __restri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x / 32;
   const int groups = words / 4;  // 128-key tiles per row (words is a multiple of 4)
-  const int oct = lane & 7;
   for (int row = blockIdx.y; row < C; row += gridDim.y) {
     if (threadIdx.x == 0) kept_any = 0;
     for (int t = threadIdx.x; t < 64; t += blockDim.x) row_tiles[t] = 0u;
@@ -967,8 +984,47 @@ __global__ void __launch_bounds__(256) mask_pack_vec_kernel(const void* __restri
     const long long rbase = (long long)row * ld;
     for (int m0 = warp * kPackGroups; m0 < groups; m0 += nwarps * kPackGroups) {
       float v[kPackGroups][4];
+      // uniform: every key of the round's kPackGroups tiles exists (all rounds but those at a row's end)
+      if ((m0 + kPackGroups) * kTile <= T) {
 #pragma unroll
-      for (int u = 0; u < kPackGroups; ++u) {  // every load first, then the shuffles
+        for (int u = 0; u < kPackGroups; ++u) {  // every load first, then the ballots
+          const long long o = rbase + (m0 + u) * kTile + 4 * lane;
+          if (f16) {
+            const uint2 r = __ldcs(reinterpret_cast<const uint2*>(static_cast<const __half*>(mask) + o));
+            v[u][0] = __half2float(__ushort_as_half((unsigned short)(r.x & 0xFFFFu)));
+            v[u][1] = __half2float(__ushort_as_half((unsigned short)(r.x >> 16)));
+            v[u][2] = __half2float(__ushort_as_half((unsigned short)(r.y & 0xFFFFu)));
+            v[u][3] = __half2float(__ushort_as_half((unsigned short)(r.y >> 16)));
+          } else {
+            const float4 r = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(mask) + o));
+            v[u][0] = r.x;
+            v[u][1] = r.y;
+            v[u][2] = r.z;
+            v[u][3] = r.w;
+          }
+        }
+        uint32_t kept_tiles = 0u;  // bit u: tile m0 + u keeps a key
+#pragma unroll
+        for (int u = 0; u < kPackGroups; ++u) {
+          uint32_t wc[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            nonbin |= !(v[u][c] == 0.f || v[u][c] <= -10000.f);
+            wc[c] = __ballot_sync(0xffffffffu, v[u][c] == 0.f);
+          }
+          if (lane == 0)
+            *reinterpret_cast<uint4*>(bits + (long long)row * words + 4 * (m0 + u)) =
+                make_uint4(wc[0], wc[1], wc[2], wc[3]);
+          kept_tiles |= ((wc[0] | wc[1] | wc[2] | wc[3]) != 0u) ? (1u << u) : 0u;
+        }
+        any |= kept_tiles != 0u;
+        // the round's four tiles share one bitmap word (m0 is a multiple of 4)
+        if (lane == 0 && tiles != nullptr && kept_tiles != 0u)
+          atomicOr(&row_tiles[m0 >> 5], kept_tiles << (m0 & 31));
+        continue;
+      }
+#pragma unroll
+      for (int u = 0; u < kPackGroups; ++u) {  // the row's last round: ragged or missing tiles
         const int key0 = (m0 + u) * kTile + 4 * lane;
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[u][c] = 0.f;
@@ -999,20 +1055,24 @@ __global__ void __launch_bounds__(256) mask_pack_vec_kernel(const void* __restri
       for (int u = 0; u < kPackGroups; ++u) {
         const int m = m0 + u;
         if (m >= groups) break;  // uniform across the warp
-        const int key0 = m * kTile + 4 * lane;
-        uint32_t nib = 0u;
+        uint32_t wc[4];
+        if ((m + 1) * kTile <= T) {  // uniform: every key of the tile exists
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const bool inb = key0 + c < T;
-          nonbin |= inb && !(v[u][c] == 0.f || v[u][c] <= -10000.f);
-          nib |= (inb && v[u][c] == 0.f) ? (1u << c) : 0u;
+          for (int c = 0; c < 4; ++c) {
+            nonbin |= !(v[u][c] == 0.f || v[u][c] <= -10000.f);
+            wc[c] = __ballot_sync(0xffffffffu, v[u][c] == 0.f);
+          }
+        } else {  // the row's ragged last tile
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const bool inb = m * kTile + 4 * lane + c < T;
+            nonbin |= inb && !(v[u][c] == 0.f || v[u][c] <= -10000.f);
+            wc[c] = __ballot_sync(0xffffffffu, inb && v[u][c] == 0.f);
+          }
         }
-        uint32_t word = nib << (4 * oct);
-        word |= __shfl_xor_sync(0xffffffffu, word, 1);
-        word |= __shfl_xor_sync(0xffffffffu, word, 2);
-        word |= __shfl_xor_sync(0xffffffffu, word, 4);
-        if (oct == 0) bits[(long long)row * words + 4 * m + (lane >> 3)] = word;
-        const bool tile_kept = __any_sync(0xffffffffu, nib != 0u);
+        if (lane == 0)
+          *reinterpret_cast<uint4*>(bits + (long long)row * words + 4 * m) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
+        const bool tile_kept = (wc[0] | wc[1] | wc[2] | wc[3]) != 0u;
         any |= tile_kept;
         if (lane == 0 && tiles != nullptr && tile_kept) atomicOr(&row_tiles[m >> 5], 1u << (m & 31));
       }

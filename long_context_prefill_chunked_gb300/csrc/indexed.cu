@@ -24,9 +24,28 @@ __device__ __forceinline__ void set_key_range(uint32_t* rw, int k0, int k1) {
   }
 }
 
-// One CTA per row (rows past the grid loop): the row's bits are built in shared memory, then
-// written 16 bytes (one 128-key tile) per thread; a warp's 32 consecutive tiles become one
-// tile-bitmap word through a ballot.
+// Bits 0, 4, ..., 28 of x moved to bits 0 .. 7.
+__device__ __forceinline__ uint32_t every_fourth(uint32_t x) {
+  x &= 0x11111111u;
+  x = (x | (x >> 3)) & 0x03030303u;
+  x = (x | (x >> 6)) & 0x000F000Fu;
+  return (x | (x >> 12)) & 0x000000FFu;
+}
+
+// A 128-key tile's bits in key order (bit i of word q = key 32q + i) in the packed-mask layout
+// the attention kernel reads (bit L of word c = key 4L + c).
+__device__ __forceinline__ uint4 to_packed_layout(const uint32_t (&o)[4]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    w[c] = every_fourth(o[0] >> c) | (every_fourth(o[1] >> c) << 8) | (every_fourth(o[2] >> c) << 16) |
+           (every_fourth(o[3] >> c) << 24);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One CTA per row (rows past the grid loop): the row's bits are built in key order in shared
+// memory, then written 16 bytes (one 128-key tile) per thread in the packed-mask layout; a
+// warp's 32 consecutive tiles become one tile-bitmap word through a ballot.
 __global__ void __launch_bounds__(256) index_pack_kernel(const int32_t* __restrict__ keep_idx,
                                                          const int32_t* __restrict__ keep_cnt,
                                                          long long stride, int ratio, int C, int s,
@@ -60,7 +79,8 @@ __global__ void __launch_bounds__(256) index_pack_kernel(const int32_t* __restri
       const int t = t0 + threadIdx.x;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (t < n_kt) {
-        v = make_uint4(rw[4 * t], rw[4 * t + 1], rw[4 * t + 2], rw[4 * t + 3]);
+        const uint32_t o[4] = {rw[4 * t], rw[4 * t + 1], rw[4 * t + 2], rw[4 * t + 3]};
+        v = to_packed_layout(o);
         out[t] = v;
       }
       const bool seen = (v.x | v.y | v.z | v.w) != 0u;
