@@ -398,28 +398,27 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
 
 }  // namespace
 
-// One CTA per (query tile, batch x KV head), thread r = tile row r: the row's words are
-// ORed over the KV head's G query heads and written back to each; the tile's union is
-// then compacted into every head's tile list (ascending).
+// One CTA per (query tile, batch x KV head): each (row, word) element of the tile's rows is ORed
+// over the KV head's G query heads and written back to each, with consecutive threads on
+// consecutive words of the row-major bits (coalesced); the tile's union is then compacted into
+// every head's tile list (ascending).
 __global__ void __launch_bounds__(128) share_group_kernel(const IndexArgs a) {
   __shared__ uint32_t un[kMaxWords];
   const int qt = blockIdx.x;
   const int b = blockIdx.y / a.Hkv, g = blockIdx.y % a.Hkv;
   const int r = threadIdx.x, lane = r & 31;
-  const int row = qt * kTile + r;
-  const bool valid = row < a.C;
   for (int w = r; w < kMaxWords; w += blockDim.x) un[w] = 0u;
   __syncthreads();
-  for (int w = 0; w < a.words; ++w) {
+  const int rows = min(kTile, a.C - qt * kTile);
+  const int n = rows * a.words;
+  const long long head = (long long)a.C * a.words;  // one query head's bits
+  const uint32_t* src = a.row_bits + (long long)(b * a.Hq + g * a.G) * head + (long long)qt * kTile * a.words;
+  uint32_t* dst = a.row_bits + (long long)(b * a.Hq + g * a.G) * head + (long long)qt * kTile * a.words;
+  for (int e = r; e < n; e += blockDim.x) {
     uint32_t acc = 0u;
-    if (valid) {
-      for (int j = 0; j < a.G; ++j)
-        acc |= a.row_bits[((long long)(b * a.Hq + g * a.G + j) * a.C + row) * a.words + w];
-      for (int j = 0; j < a.G; ++j)
-        a.row_bits[((long long)(b * a.Hq + g * a.G + j) * a.C + row) * a.words + w] = acc;
-    }
-    const uint32_t uw = __reduce_or_sync(0xffffffffu, acc);
-    if (lane == 0 && uw) atomicOr(&un[w], uw);
+    for (int j = 0; j < a.G; ++j) acc |= src[j * head + e];
+    for (int j = 0; j < a.G; ++j) dst[j * head + e] = acc;
+    if (acc != 0u) atomicOr(&un[e % a.words], acc);
   }
   __syncthreads();
   if (r < 32) {
