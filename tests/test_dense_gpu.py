@@ -316,14 +316,16 @@ def test_binary_mask_tile_bitmap_above_1024_tiles():
 
 @pytest.mark.parametrize("mdtype", [np.float32, np.float16])
 @pytest.mark.parametrize("tail", [0.0, -30000.0, -2.0])
-def test_padded_mask_rows_with_ragged_keys(mdtype, tail):
-    """Mask rows padded to a 16-byte stride while start_pos + C = 941 is not a multiple of 4:
-    the packing pass reads the rows with vector loads and the last key of each row on its own.
+@pytest.mark.parametrize("padded", [True, False])
+def test_padded_mask_rows_with_ragged_keys(mdtype, tail, padded):
+    """start_pos + C = 941 keys per mask row, not a multiple of 4.  Rows padded to a 16-byte
+    stride: the packing pass reads them with vector loads and the last key of each row on its
+    own; contiguous rows (941 values apart, not on 16-byte boundaries): the scalar packing pass.
     The rows' last key carries `tail` in every third row (kept, dropped, or a non-binary value
     that sends the call to the value path); the padding holds NaN, which no row may read."""
     C, s = 301, 640
     T = s + C
-    ld = (T + 7) // 8 * 8 + 8
+    ld = (T + 7) // 8 * 8 + 8 if padded else T
     w = pi.normal_workload("padded-mask", 91, 1, 4, 2, 128, T, C, "bf16")
     g = np.random.default_rng(92)
     vals = np.where(g.random((C, T)) < 0.4, -30000.0, 0.0)
