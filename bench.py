@@ -388,7 +388,9 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
     block-sparse prefill (block index + sparse attention with the pooled correction, block 128,
     alpha 0.1; one pooled-key buffer and workspace for the prompt, each chunk pooling only its
     own blocks).  CUDA events per call on the launching stream; the median over `reps` passes
-    (inputs are 1.5 GB, far beyond L2).  Skip share is weighted by dense work: per (head, query
+    (inputs are 1.5 GB, far beyond L2).  The block-sparse prefill is also timed pipelined: each
+    chunk's block index on a low-priority stream ahead of the sparse attention on a high-priority
+    one (wall time, `sparse_pipelined_ms`).  Skip share is weighted by dense work: per (head, query
     tile) the dense path runs its off-diagonal key tiles plus half a diagonal tile, the sparse
     path its kept off-diagonal tiles plus the same half (pooled tiles not counted)."""
     import torch
@@ -437,6 +439,33 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
             index_t.append([a.elapsed_time(b) for a, b in e["i"]])
             attn_t.append([a.elapsed_time(b) for a, b in e["a"]])
     pfx.stream_status(stream)
+    # the same block-sparse prefill pipelined as a caller would run it: the block index of each
+    # chunk on a low-priority stream, the v conversion and sparse attention on a high-priority one
+    # (attention i waits for index i only), so the next chunks' index kernels take the SMs the
+    # attention kernel leaves idle in its last wave.  Wall time from the first call to the last.
+    hi = torch.cuda.Stream(dev, priority=-1)
+    lo = torch.cuda.Stream(dev, priority=0)
+    pipe_t = []
+    for it in range(warmup + reps):
+        e0, e1 = ev(), ev()
+        done = [torch.cuda.Event() for _ in starts]
+        e0.record(hi)
+        lo.wait_event(e0)
+        for i, s in enumerate(starts):
+            q = Q[:, s:s + C]
+            pfx.block_index(q, K[:, :s + C], s, BLOCK, ALPHA, sel=sels[i], stream=lo)
+            done[i].record(lo)
+            pfx.to_f16(V[:, s:s + C], out=v16_s[:, s:s + C], stream=hi)
+            hi.wait_event(done[i])
+            pfx.attn_sparse(q, K[:, :s + C], v16_s[:, :s + C], s, sels[i], block=BLOCK, pooled=pooled, out=out,
+                            stream=hi)
+        e1.record(hi)
+        torch.cuda.synchronize(dev)
+        if it >= warmup:
+            pipe_t.append(e0.elapsed_time(e1))
+    pfx.stream_status(hi)
+    pfx.stream_status(lo)
+    t_pipe = statistics.median(pipe_t)
     med = lambda runs: statistics.median(sum(r) for r in runs)
     t_dense, t_index, t_attn = med(dense_t), med(index_t), med(attn_t)
     t_sparse = t_index + t_attn
@@ -462,6 +491,12 @@ def run_long_128k(pfx, dev, reps=3, warmup=1):
         "efficiency": (t_dense / t_sparse) * (1.0 - skip),
         "efficiency_note": "(t_dense / t_sparse) * (1 - skip); 1 = sparse time exactly in proportion to "
                            "the dense work it keeps",
+        "sparse_pipelined_ms": t_pipe,
+        "sparse_pipelined_tflops_equiv": flops / (t_pipe * 1e-3) / 1e12,
+        "efficiency_pipelined": (t_dense / t_pipe) * (1.0 - skip),
+        "pipelined_note": "wall time of the block-sparse prefill with each chunk's block index on a "
+                          "low-priority stream and its attention on a high-priority one (attention i "
+                          "waits for index i); sparse_ms is the sum of the per-call times on one stream",
         "dense_ms_per_chunk": [statistics.median(r[i] for r in dense_t) for i in range(len(starts))],
         "sparse_ms_per_chunk": [statistics.median(a[i] + b[i] for a, b in zip(index_t, attn_t))
                                 for i in range(len(starts))],

@@ -137,6 +137,50 @@ def test_sparse_shapes_dtypes_and_batches(B, Hq, Hkv, d, dtype, s, C):
     assert oracle.skip_share(osel) > 0.3
 
 
+def test_pipelined_chunks_equal_serial():
+    """A chunked prompt with each chunk's block index on a low-priority stream ahead of the
+    sparse attention on a high-priority stream (attention i waits for index i only; the pooled
+    keys are shared and grow chunk by chunk): every chunk's output equals the one-stream run bit
+    for bit, and the last chunk matches the oracle."""
+    w = pi.planted_workload("pipelined", 33, 1, 8, 2, 128, 8192, 2048, "bf16", beta=14.0)
+    N, C = w.N, w.chunk
+    Q, K, V = dev(w.q, "bf16"), dev(w.k, "bf16"), dev(w.v, "bf16")
+    starts = list(range(0, N, C))
+    kbar = pfx.alloc_kbar(Q[:, :C], K, N, 128)
+    pooled = pfx.alloc_pooled(Q[:, :C], K, 0, 128, max_keys=N)
+    sels = [pfx.alloc_selection(Q[:, s:s + C], K[:, :s + C], s, 128, kbar=kbar, pooled_blocks=s // 128)
+            for s in starts]
+    outs = {m: torch.empty((len(starts), 1, C, 8, 128), dtype=torch.float32, device="cuda")
+            for m in ("serial", "pipelined")}
+    for i, s in enumerate(starts):
+        pfx.block_index(Q[:, s:s + C], K[:, :s + C], s, 128, 0.1, sel=sels[i])
+        pfx.attn_sparse(Q[:, s:s + C], K[:, :s + C], V[:, :s + C], s, sels[i], pooled=pooled,
+                        out=outs["serial"][i])
+    torch.cuda.synchronize()
+    hi = torch.cuda.Stream(priority=-1)
+    lo = torch.cuda.Stream(priority=0)
+    start = torch.cuda.Event()
+    start.record(torch.cuda.current_stream())
+    hi.wait_event(start)
+    lo.wait_event(start)
+    for i, s in enumerate(starts):
+        pfx.block_index(Q[:, s:s + C], K[:, :s + C], s, 128, 0.1, sel=sels[i], stream=lo)
+        done = torch.cuda.Event()
+        done.record(lo)
+        hi.wait_event(done)
+        pfx.attn_sparse(Q[:, s:s + C], K[:, :s + C], V[:, :s + C], s, sels[i], pooled=pooled,
+                        out=outs["pipelined"][i], stream=hi)
+    torch.cuda.synchronize()
+    pfx.stream_status(hi)
+    pfx.stream_status(lo)
+    assert torch.equal(outs["serial"], outs["pipelined"])
+    s = starts[-1]
+    rows = sample_rows(C, 96, 34)
+    ref, osel, gk = expected_sparse(w, s, C, 0.1, rows, sels[-1])
+    check_selection(osel, gk)
+    assert_rows_close(outs["pipelined"][-1][:, rows], ref, "pipelined last chunk")
+
+
 def test_near_threshold_pairs_on_the_gpu(small):
     """alpha is set to one candidate's own probability ratio (rounded to fp32), so that pair --
     and any other within 1e-4 relative -- sits in the threshold band.  The GPU may decide it
